@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Throughput of the DSA hot path (fused Lightning Indexer top-K + Sparse Flash Attention).
+
+One step = one pass of the whole path over one batch: li_topk then sfa_decode (sfa_prefill for
+the prefill workload), launched through the C ABI.  Default workload: decode, 32 sequences x 1
+token at 32768 context, 64x128 index heads, top-2048, 128 attention heads over the 576/512 MLA
+latent cache (bf16).
+
+Prints ONE JSON line (rank 0):
+  value      tokens/s over all ranks, inputs resident in HBM (max over ranks of the timed region)
+  e2e        the same through host buffers: per step, the step's query-side inputs are copied
+             host->device from pinned memory and the outputs device->host, inside the timed region
+  roofline   the dominant kernel (li_topk): algorithmic bytes per launch / its mean CUDA-event
+             duration vs the measured HBM copy bandwidth; traffic from the committed ncu summary
+  cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the same workload
+Multi-GPU (torchrun): every rank runs its own independently seeded batch (weak scaling, no
+collective on the data path).  ``--impl reference`` times the CPU oracle instead.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LI+SFA decode tokens/sec at 32k ctx; achieved HBM GB/s vs ~8 TB/s peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_32k")
+    ap.add_argument("--baseline-seconds", type=float, default=15.0,
+                    help="CPU oracle sample budget for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- bytes / flops
+
+def algorithmic(wl, cnt_total):
+    """Per-step algorithmic work: key pages every token's visible range touches (read once per
+    sequence), gathered latent rows (one 1152-byte row per selected index), FLOPs."""
+    P = wl.page_size
+    elt = 1 if wl.li_dtype == "fp8" else 2
+    pages = sum(math.ceil(L / P) for L in wl.seq_lens)
+    k_bytes = pages * P * wl.d_I * elt + (pages * P * 4 if wl.li_dtype == "fp8" else 0)
+    gather_bytes = cnt_total * wl.d_qk * 2
+    li_flop = 0
+    for L, n in zip(wl.seq_lens, wl.n_new):
+        li_flop += sum(2 * (L - n + i + 1) * wl.H_I * wl.d_I for i in range(n))
+    sfa_flop = cnt_total * wl.H * (wl.d_qk + wl.d_v) * 2
+    return {"k_bytes": k_bytes, "gather_bytes": gather_bytes, "metric_bytes": k_bytes + gather_bytes,
+            "li_flop": li_flop, "sfa_flop": sfa_flop}
+
+
+# ----------------------------------------------------------------------------- clocks (NVML)
+
+class ClockSampler:
+    """Polls SM clock and clock-event reasons through NVML (ctypes) while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting"}
+
+    def __init__(self, pci_bus_id):
+        self.ok = False
+        self.samples, self.reasons = [], 0
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if pci_bus_id is None or self.nv.nvmlDeviceGetHandleByPciBusId_v2(
+                    pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+                if self.nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _poll(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0:
+                self.samples.append(c.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r)) == 0:
+                self.reasons |= r.value
+            time.sleep(0.0005)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples),
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b]}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def committed_traffic(workload):
+    """Per-launch DRAM bytes of li_topk from the committed ncu summary, if the kernel source is
+    unchanged since it was taken (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "dsa_sparse_attention_li_gb300", "csrc", e["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return e["dram_bytes_per_launch"] if sha == e["source_sha256_16"] else None
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_rate(inp_cpu, budget_s, tokens_per_call=None):
+    """Tokens/s of the oracle (indexer top-K + attention on its own selection) over a bounded
+    sample of the workload's tokens."""
+    import numpy as np
+    import oracle
+    wl = inp_cpu["wl"]
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    n = tokens_per_call or min(wl.n_q, max(1, cores))
+    rng = np.random.default_rng(5)
+    done, t_total, calls = 0, 0.0, 0
+    while t_total < budget_s:
+        toks = sorted(rng.choice(wl.n_q, size=n, replace=False).tolist())
+        t0 = time.perf_counter()
+        idx, _, _ = oracle.li_topk(inp_cpu, toks)
+        oracle.sfa(inp_cpu, idx, toks)
+        t_total += time.perf_counter() - t0
+        done += n
+        calls += 1
+    return done / t_total, cores, "%d calls x %d tokens of %s (%.1f s)" % (calls, n, wl.name, t_total)
+
+
+def run_reference(args):
+    """The CPU oracle as it stands, on this host's cores: each step runs the whole path (indexer
+    full-sort top-K, then attention on that selection) for a bounded sample of the workload's
+    query tokens, sized so that warm-up + timed steps take about two minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import dsa_inputs as di
+    import oracle
+    wl = di.preset(args.workload)
+    inp_cpu = di.generate(wl, device="cpu")
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    rng = np.random.default_rng(5)
+
+    def call(n):
+        toks = sorted(rng.choice(wl.n_q, size=n, replace=False).tolist())
+        t0 = time.perf_counter()
+        idx, _, _ = oracle.li_topk(inp_cpu, toks)
+        oracle.sfa(inp_cpu, idx, toks)
+        return time.perf_counter() - t0
+
+    t_one = call(1)  # calibration (part of the warm-up)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(wl.n_q, cores * max(1, math.floor(budget / max(t_one, 1e-6))))))
+    for _ in range(max(0, args.warmup - 1)):
+        call(n)
+    times = [call(n) for _ in range(max(1, args.steps))]
+    value = n * len(times) / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * statistics.mean(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": wl.describe(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: the fp64 oracle (indexer full-sort top-K + "
+                                       "direct softmax attention) on %d of the %d query tokens"
+                                       % (n, wl.n_q)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import dsa_inputs as di
+    import dsa_sparse_attention_li_gb300 as dsa
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    lib = dsa.load()
+
+    wl = di.preset(args.workload)
+    if world > 1:
+        wl = di.Workload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
+    prefill = max(wl.n_new) > 2
+    inp = di.generate(wl, device=dev)
+    n_q = wl.n_q
+    ms, mq = max(wl.seq_lens), max(wl.n_new)
+    idx = torch.empty((n_q, wl.K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((n_q,), dtype=torch.int32, device=dev)
+    out = torch.empty((n_q, wl.H, wl.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((n_q, wl.H), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = None if prefill else dsa.new_workspace(dsa.sfa_workspace_bytes(inp["q_sfa"], idx), dev)
+    li_args = dsa.li_topk_args(inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"],
+                               inp["q_start"], wl.K, q_scale=inp.get("q_scale"),
+                               k_scale=inp.get("k_scale"), max_seq_len=ms, max_q_per_seq=mq,
+                               out_idx=idx, out_cnt=cnt, status=status)
+    sfa_args = dsa.sfa_args(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"],
+                            inp["q_start"], idx, softmax_scale=wl.softmax_scale, max_seq_len=ms,
+                            max_q_per_seq=mq, out=out, lse=lse, status=status, workspace=ws)
+    stream = torch.cuda.Stream(device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    sfa_entry = lib.dsa_sfa_prefill if prefill else lib.dsa_sfa_decode
+
+    def step():
+        rc = lib.dsa_li_topk(ctypes.byref(li_args), sp)
+        rc |= sfa_entry(ctypes.byref(sfa_args), sp)
+        if rc:
+            raise RuntimeError("launch failed: " + dsa.last_error())
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(status.item()))
+    cnt_total = int(cnt.sum().item())
+    work = algorithmic(wl, cnt_total)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    e_all = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    pci = None
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        pci = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(pci) as clk:
+        with torch.cuda.stream(stream):
+            e_all[0].record(stream)
+            for i in range(K):
+                ev[i][0].record(stream)
+                lib.dsa_li_topk(ctypes.byref(li_args), sp)
+                ev[i][1].record(stream)
+                sfa_entry(ctypes.byref(sfa_args), sp)
+                ev[i][2].record(stream)
+            e_all[1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = e_all[0].elapsed_time(e_all[1])
+    li_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    sfa_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the timed region" % int(status.item()))
+    t = torch.tensor([total_ms], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(t.item())
+    value = n_q * world * K / (total_ms / 1000.0)
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        names = ["q_li", "q_scale", "w", "q_sfa", "pt_k", "pt_kv", "seq_lens", "q_start"]
+        host = {k: inp[k].cpu().pin_memory() for k in names if inp.get(k) is not None}
+        outs = {"idx": idx, "out": out, "lse": lse}
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+        K2 = max(3, K // 4)
+        with torch.cuda.stream(stream):
+            for it in range(K2 + 2):
+                if it == 2:
+                    torch.cuda.synchronize()
+                    if world > 1:
+                        torch.distributed.barrier()
+                    t0 = time.perf_counter()
+                for k, v in host.items():
+                    inp[k].copy_(v, non_blocking=True)
+                step()
+                for k, v in outs.items():
+                    host_out[k].copy_(v, non_blocking=True)
+            stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+        t = torch.tensor([e2e_s], device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e = {"value": n_q * world * K2 / float(t.item()), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    hbm, tf, peak_kind = measured_peaks()
+    li_achieved = work["k_bytes"] / (li_ms / 1000.0) / 1e9
+    step_gbs = work["metric_bytes"] / (total_ms / K / 1000.0) / 1e9
+    traffic = committed_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8" if wl.li_dtype == "fp8" else "bf16",
+        "data": "synthetic",
+        "config": {**wl.describe(), "l2": "inputs larger than L2: every step streams %.0f MB of key pages "
+                   "and gathers from a %.0f MB latent pool" % (work["k_bytes"] / 1e6,
+                                                               inp["kv_pool"].numel() * 2 / 1e6),
+                   "launch": "eager C-ABI calls on one stream, CUDA events between kernels"},
+        "roofline": {"kernel": "li_topk", "bound": "hbm", "achieved": li_achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": li_achieved / hbm, "peak_kind": peak_kind,
+                     "traffic": traffic, "algorithmic_bytes": work["k_bytes"]},
+        "step_hbm": {"metric_bytes": work["metric_bytes"], "achieved_gbs": step_gbs,
+                     "frac": step_gbs / hbm, "peak_kind": peak_kind},
+        "kernels": {"li_topk_us": li_ms * 1000.0, "sfa_us": sfa_ms * 1000.0,
+                    "li_topk_gbs": li_achieved,
+                    "sfa_gbs": work["gather_bytes"] / (sfa_ms / 1000.0) / 1e9,
+                    "sfa_tflops": work["sfa_flop"] / (sfa_ms / 1000.0) / 1e12,
+                    "li_tflops": work["li_flop"] / (li_ms / 1000.0) / 1e12},
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        inp_cpu = di.to_device(inp, "cpu")
+        rate, cores, sample = oracle_sample_rate(inp_cpu, args.baseline_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

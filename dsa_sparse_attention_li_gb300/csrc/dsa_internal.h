@@ -1,0 +1,43 @@
+// dsa_internal.h -- host-side declarations shared by the C-ABI front end and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <string>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// Launchers: arguments are already validated by the front end (api.cu).
+dsa_status launch_li_topk(const dsa_li_args& a, cudaStream_t stream, std::string& err);
+dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, std::string& err);
+size_t sfa_workspace_bytes(const dsa_sfa_args& a);
+dsa_status launch_cache_write(void* pool, float* scale_pool, int num_pages, int page_size, int dim,
+                              int elem_bytes, const int32_t* page_table, int max_pages, int B,
+                              const int32_t* seq, const int32_t* pos, const void* rows,
+                              const float* row_scales, int n_rows, int32_t* status,
+                              cudaStream_t stream, std::string& err);
+
+// 2-D tiled TMA descriptor over a row-major [outer][inner] array (inner contiguous).
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                    uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                    uint32_t box_outer, CUtensorMapSwizzle swizzle, std::string& err);
+
+// Device properties of the current device (cached per device).
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int smem_optin = 0;   // max dynamic shared memory per block
+  int smem_per_sm = 0;  // shared memory per multiprocessor
+  int cc_major = 0, cc_minor = 0;
+};
+bool device_info(DeviceInfo& info, std::string& err);
+
+inline dsa_status cuda_fail(cudaError_t e, const char* what, std::string& err) {
+  err = std::string(what) + ": " + cudaGetErrorString(e);
+  return DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

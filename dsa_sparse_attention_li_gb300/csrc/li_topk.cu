@@ -1,0 +1,696 @@
+// li_topk.cu -- fused Lightning Indexer: score contraction on tcgen05 tensor cores, head-weighted
+// ReLU reduction in the epilogue, and an exact cluster-wide radix top-K select in shared memory.
+// Only the selected positions leave the chip.
+//
+// Method: "Inference Optimization for Kimi K3.1 Pro: Decoding Architecture Evolution and Systems
+// Engineering Practices", section 1 (DSA steps 1-2: indexer scoring with head weights, top-K) and
+// section 2 (Operator-Level Deep Fusion: score, head weighting and top-K in one kernel, scores
+// kept on chip, indices then drive paged reads); "Day0 Inference Adaptation for Next-Gen LLMs ...
+// CANN", section 3.1 (the indexer reads the paged key cache directly; prefill and decode, BF16
+// and quantised paths).
+//
+// Work decomposition.  One thread-block cluster of C CTAs serves one (sequence, group of T query
+// tokens).  CTA r of the cluster owns the key positions [r*chunk, (r+1)*chunk) of the sequence:
+//   streaming phase  warp 0 issues TMA loads of two 64-row key pages per 128-key tile (page ids
+//                    resolved through the page table), warp 1 issues tcgen05.mma
+//                    D[128 keys x T*H_I] = K_tile . Q^T into a double-buffered TMEM accumulator,
+//                    warps 4..7 (one TMEM lane = one key per thread) apply ReLU, the head weights
+//                    and the head sum, mask by causality and length, and store an order-preserving
+//                    32-bit key of each score in shared memory;
+//   select phase     three radix passes (11/11/10 bits) build per-CTA histograms whose cluster
+//                    total is read over distributed shared memory; every CTA derives the same
+//                    K-th key and the number of ties to take; per-CTA counts give each CTA its
+//                    output offset and tie quota (ties go to the lowest positions, CTAs own
+//                    ascending position ranges), and a ballot compaction writes the positions in
+//                    ascending order.
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+
+#include "dsa_internal.h"
+#include "ptx.cuh"
+
+namespace dsa {
+namespace li {
+
+constexpr int kThreads = 256;
+constexpr int kTileKeys = 128;
+constexpr int kHistWords = 1024;  // 2048 radix bins, two 16-bit counters per 32-bit word
+constexpr int kMaxCluster = 16;
+
+struct Params {
+  int B, n_q, K, max_pages, num_pages;
+  int groups;  // token groups per sequence
+  int chunk;   // key positions per CTA (multiple of 128)
+  int C;       // cluster size
+  int nstage;  // TMA ring depth
+  const float* w;
+  const float* q_scale;
+  const float* k_scale;
+  const int* page_table;
+  const int* seq_lens;
+  const int* q_start;
+  int* out_idx;
+  int* out_cnt;
+  int* status;
+  const void* q;       // raw pointers (used by the CUDA-core scoring variant only)
+  const void* k_pool;
+};
+
+template <int D_I, bool FP8, int H_I, int T>
+struct Cfg {
+  static constexpr int kElt = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D_I * kElt;      // 128 or 256
+  static constexpr int kBoxes = kRowBytes / 128;    // 128-byte column boxes per row
+  static constexpr int kKSteps = kRowBytes / 32;    // one MMA consumes 32 bytes of K
+  static constexpr int kNCol = (T * H_I < 16) ? 16 : T * H_I;  // MMA N (>= 16 for M = 128)
+  static constexpr int kTileBytes = kTileKeys * kRowBytes;
+  static constexpr int kQBytes = kNCol * kRowBytes;
+  static constexpr int kTmemCols = (2 * kNCol <= 32)    ? 32
+                                   : (2 * kNCol <= 64)  ? 64
+                                   : (2 * kNCol <= 128) ? 128
+                                   : (2 * kNCol <= 256) ? 256
+                                                        : 512;
+  static_assert(kNCol % 16 == 0 && kNCol <= 256, "MMA N");
+  static_assert(T * H_I <= 256, "tokens x heads per group");
+};
+
+// Shared memory carve-up (offsets from a 1024-byte aligned base).
+struct Layout {
+  int stages, q, wts, scores, hist, pages, ctl, total;
+  __host__ __device__ Layout(int nstage, int tile_bytes, int q_bytes, int T, int H_I, int chunk) {
+    stages = 0;
+    q = stages + nstage * tile_bytes;
+    wts = q + q_bytes;
+    scores = wts + ((T * H_I * 4 + 127) / 128) * 128;
+    hist = scores + T * chunk * 4;
+    pages = hist + 2 * T * kHistWords * 4;
+    ctl = pages + ((2 * (chunk / kTileKeys) * 4 + 127) / 128) * 128;
+    total = ctl + 1024;
+  }
+};
+
+struct Ctl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t qbar;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  uint32_t scan[8];
+  int need[4];        // remaining count to select among the current prefix
+  uint32_t prefix[4]; // key prefix fixed so far
+  int radix[4];       // token needs a radix select (visible > K)
+  int need_total[4];  // min(K, visible)
+  int cnt_gt[4], cnt_eq[4];  // this CTA's counts (read by the cluster)
+  int offset[4], quota[4];
+  int found_bin[4], found_need[4];
+};
+
+// ---- block-level scans over 256 threads ----
+
+// Exclusive suffix sum: sum of v over threads with a larger index.
+DSA_DEV uint32_t block_excl_suffix(uint32_t v, uint32_t* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  if (lane == 0) scratch[warp] = x;
+  __syncthreads();
+  uint32_t above = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w)
+    if (w > warp) above += scratch[w];
+  __syncthreads();
+  return above + x - v;
+}
+
+// Exclusive prefix counts of two flags at once; totals returned through tot_a / tot_b.
+DSA_DEV void block_excl_flags(bool fa, bool fb, uint32_t* scratch, uint32_t& pa, uint32_t& pb,
+                              uint32_t& tot_a, uint32_t& tot_b) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t ma = __ballot_sync(0xffffffffu, fa), mb = __ballot_sync(0xffffffffu, fb);
+  const uint32_t lt = (1u << lane) - 1u;
+  if (lane == 0) scratch[warp] = (uint32_t)__popc(ma) | ((uint32_t)__popc(mb) << 16);
+  __syncthreads();
+  uint32_t ba = 0, bb = 0, ta = 0, tb = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t c = scratch[w];
+    if (w < warp) {
+      ba += c & 0xffffu;
+      bb += c >> 16;
+    }
+    ta += c & 0xffffu;
+    tb += c >> 16;
+  }
+  __syncthreads();
+  pa = ba + __popc(ma & lt);
+  pb = bb + __popc(mb & lt);
+  tot_a = ta;
+  tot_b = tb;
+}
+
+DSA_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+DSA_DEV float e4m3_to_float(uint8_t b) {
+  __nv_fp8_e4m3 v;
+  v.__x = b;
+  return float(v);
+}
+
+// ---- the fused kernel ----
+
+template <int D_I, bool FP8, int H_I, int T, bool kTensorCore>
+__global__ void __launch_bounds__(kThreads, 1)
+    li_topk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                   const Params p) {
+  using CF = Cfg<D_I, FP8, H_I, T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const Layout lay(p.nstage, CF::kTileBytes, CF::kQBytes, T, H_I, p.chunk);
+  uint8_t* stage_base = smem + lay.stages;
+  uint8_t* q_s = smem + lay.q;
+  float* wts = reinterpret_cast<float*>(smem + lay.wts);
+  uint32_t* scores = reinterpret_cast<uint32_t*>(smem + lay.scores);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + lay.hist);
+  int* pages = reinterpret_cast<int*>(smem + lay.pages);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + lay.ctl);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = (int)cluster_rank();
+  const int cl = blockIdx.x / p.C;
+  const int b = cl / p.groups, g = cl % p.groups;
+  if (b >= p.B) return;
+  const int qs = p.q_start[b];
+  const int n_b = p.q_start[b + 1] - qs;
+  const int L = p.seq_lens[b];
+  // Cluster-uniform validity (every CTA of the cluster reads the same values).
+  if (g == p.groups - 1 && rank == 0 && tid == 0 && n_b > p.groups * T)
+    report(p.status, kStatusDeviceCheck);
+  if (n_b < 0 || L < n_b || L > p.C * p.chunk || qs < 0 || qs + n_b > p.n_q) {
+    if (rank == 0 && tid == 0) report(p.status, kStatusDeviceCheck);
+    return;
+  }
+  const int nt = min(T, n_b - g * T);
+  if (nt <= 0) return;
+  const int t0 = qs + g * T;
+  const int pos0 = L - n_b + g * T;  // position of token t0
+  const int lo = rank * p.chunk;
+  const int hi = min(lo + p.chunk, pos0 + nt);
+  const int ntile = hi > lo ? (hi - lo + kTileKeys - 1) / kTileKeys : 0;
+  const int nscan = min(ntile * kTileKeys, p.chunk);
+  const int npages_seq = (L + 63) / 64;
+
+  // ---------------- setup
+  if (tid == 0) {
+    for (int s = 0; s < p.nstage; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tfull[a], 1);
+      mbar_init(&ctl->tempty[a], 128);
+    }
+    mbar_init(&ctl->qbar, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (kTensorCore && warp == 1) {
+    tmem_alloc(&ctl->tmem_base, CF::kTmemCols);
+    tmem_relinquish();
+  }
+  // physical page of every 64-row half tile of this CTA's range (-1 = past the sequence)
+  for (int i = tid; i < 2 * ntile; i += kThreads) {
+    const int P = lo / 64 + i;
+    int id = -1;
+    if (P < npages_seq) {
+      id = p.page_table[(size_t)b * p.max_pages + P];
+      if (id < 0 || id >= p.num_pages) {
+        report(p.status, kStatusDeviceCheck);
+        id = 0;  // stay in bounds; results for this token are then unspecified
+      }
+    }
+    pages[i] = id;
+  }
+  for (int i = tid; i < T * H_I; i += kThreads) {
+    const int tt = i / H_I, h = i % H_I;
+    float v = 0.f;
+    if (tt < nt) {
+      v = p.w[(size_t)(t0 + tt) * H_I + h];
+      if (FP8) v *= p.q_scale[(size_t)(t0 + tt) * H_I + h];
+    }
+    wts[i] = v;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  volatile int* abort = &ctl->abort;
+
+  // ---------------- streaming phase: scores of [lo, lo + nscan) into shared memory
+  if constexpr (kTensorCore) {
+    const uint32_t tmem = ctl->tmem_base;
+    if (warp == 0 && lane == 0 && ntile > 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_q);
+      mbar_arrive_expect_tx(&ctl->qbar, CF::kQBytes);
+      for (int bx = 0; bx < CF::kBoxes; ++bx)
+        tma_load_2d(q_s + bx * CF::kNCol * 128, &tm_q, &ctl->qbar, bx * (128 / CF::kElt),
+                    t0 * H_I);
+      for (int i = 0; i < ntile; ++i) {
+        const int s = i % p.nstage;
+        const uint32_t ph = (uint32_t)(i / p.nstage) & 1u;
+        if (i >= p.nstage && !mbar_wait(&ctl->empty[s], ph ^ 1u, abort, p.status)) break;
+        const int pg0 = pages[2 * i], pg1 = pages[2 * i + 1];
+        const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * CF::kBoxes * 64 * 128;
+        mbar_arrive_expect_tx(&ctl->full[s], bytes);
+        uint8_t* st = stage_base + (size_t)s * CF::kTileBytes;
+        for (int bx = 0; bx < CF::kBoxes; ++bx) {
+          const int x = bx * (128 / CF::kElt);
+          if (pg0 >= 0) tma_load_2d(st + bx * 16384, &tm_k, &ctl->full[s], x, pg0 * 64);
+          if (pg1 >= 0) tma_load_2d(st + bx * 16384 + 8192, &tm_k, &ctl->full[s], x, pg1 * 64);
+        }
+      }
+      // never leave with copies in flight: wait for the last fill of every stage
+      for (int i = max(0, ntile - p.nstage); i < ntile; ++i) {
+        const int s = i % p.nstage;
+        mbar_wait(&ctl->full[s], (uint32_t)(i / p.nstage) & 1u, abort, p.status);
+      }
+    } else if (warp == 1 && lane == 0 && ntile > 0) {
+      constexpr uint32_t idesc =
+          FP8 ? idesc_e4m3(128, CF::kNCol) : idesc_bf16(128, CF::kNCol);
+      const uint32_t q_addr = smem_u32(q_s);
+      const uint32_t st_addr = smem_u32(stage_base);
+      bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
+      for (int i = 0; ok && i < ntile; ++i) {
+        const int s = i % p.nstage;
+        const uint32_t ph = (uint32_t)(i / p.nstage) & 1u;
+        const int a = i & 1;
+        if (!mbar_wait(&ctl->full[s], ph, abort, p.status)) break;
+        if (i >= 2 && !mbar_wait(&ctl->tempty[a], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort, p.status))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(a * CF::kNCol);
+#pragma unroll
+        for (int kk = 0; kk < CF::kKSteps; ++kk) {
+          const uint32_t box = (uint32_t)(kk * 32) / 128u, off = (uint32_t)(kk * 32) % 128u;
+          const uint64_t ad = sdesc_sw128(st_addr + (uint32_t)s * CF::kTileBytes + box * 16384u + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(q_addr + box * (uint32_t)(CF::kNCol * 128) + off, 16, 1024);
+          if (FP8)
+            mma_f8_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+          else
+            mma_f16_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&ctl->empty[s]);
+        mma_commit(&ctl->tfull[a]);
+      }
+      // all MMAs retired before the accumulator is released
+      mma_commit(&ctl->drain);
+      mbar_wait(&ctl->drain, 0, abort, p.status);
+    } else if (warp >= 4) {
+      const int qd = warp - 4;  // TMEM lane quadrant of this warp
+      const int row = qd * 32 + lane;
+      for (int i = 0; i < ntile; ++i) {
+        const int a = i & 1;
+        const int j = lo + i * kTileKeys + row;
+        float ks = 1.f;
+        if (FP8) {
+          const int pg = pages[2 * i + (row >> 6)];
+          ks = pg >= 0 ? p.k_scale[(size_t)pg * 64 + (row & 63)] : 0.f;
+        }
+        const bool ok = mbar_wait(&ctl->tfull[a], (uint32_t)(i >> 1) & 1u, abort, p.status);
+        if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.ld below needs the whole warp
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(a * CF::kNCol);
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) {
+          float s = 0.f;
+          if constexpr (H_I == 64) {
+            uint32_t r[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              tmem_ld_x32(taddr + (uint32_t)(tt * H_I + half * 32), r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int h = 0; h < 32; ++h)
+                s = fmaf(wts[tt * H_I + half * 32 + h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+            }
+          } else {
+            uint32_t r[8];
+            tmem_ld_x8(taddr + (uint32_t)(tt * H_I), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+              s = fmaf(wts[tt * H_I + h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+          }
+          if (FP8) s *= ks;
+          const bool valid = tt < nt && j < lo + p.chunk && j <= pos0 + tt;
+          if (j - lo < p.chunk) scores[tt * p.chunk + (j - lo)] = valid ? score_key(s) : 0u;
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->tempty[a]);
+      }
+    }
+  } else {
+    // CUDA-core scoring (debug variant of the same kernel: identical select phase)
+    for (int e = tid; e < nscan; e += kThreads) {
+      const int j = lo + e;
+      const int pg = pages[e >> 6];
+      const size_t row = (size_t)(pg < 0 ? 0 : pg) * 64 + (j & 63);
+      float ks = 1.f;
+      if (FP8) ks = p.k_scale[row];
+      for (int tt = 0; tt < T; ++tt) {
+        float s = 0.f;
+        for (int h = 0; h < H_I; ++h) {
+          float dot = 0.f;
+          for (int d = 0; d < D_I; ++d) {
+            float qv, kv;
+            if (FP8) {
+              qv = e4m3_to_float(((const uint8_t*)p.q)[((size_t)(t0 + tt) * H_I + h) * D_I + d]);
+              kv = e4m3_to_float(((const uint8_t*)p.k_pool)[row * D_I + d]);
+            } else {
+              qv = bf16_bits_to_float(((const uint16_t*)p.q)[((size_t)(t0 + tt) * H_I + h) * D_I + d]);
+              kv = bf16_bits_to_float(((const uint16_t*)p.k_pool)[row * D_I + d]);
+            }
+            dot = fmaf(qv, kv, dot);
+          }
+          s = fmaf(wts[tt * H_I + h], fmaxf(dot, 0.f), s);
+        }
+        if (FP8) s *= ks;
+        const bool valid = tt < nt && pg >= 0 && j <= pos0 + tt;
+        scores[tt * p.chunk + e] = valid ? score_key(s) : 0u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (kTensorCore && warp == 1) {
+    __syncwarp();
+    tmem_dealloc(ctl->tmem_base, CF::kTmemCols);
+  }
+
+  // ---------------- select phase (cluster-uniform control flow)
+  if (tid < T) {
+    const int tt = tid;
+    const int vis = pos0 + tt + 1;
+    ctl->need_total[tt] = tt < nt ? min(p.K, vis) : 0;
+    ctl->radix[tt] = (tt < nt && vis > p.K) ? 1 : 0;
+    ctl->need[tt] = ctl->need_total[tt];
+    ctl->prefix[tt] = 0u;
+  }
+  __syncthreads();
+  bool any_radix = false;
+#pragma unroll
+  for (int tt = 0; tt < T; ++tt) any_radix |= ctl->radix[tt] != 0;
+
+  if (any_radix) {
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nbits = pass == 2 ? 10 : 11;
+      const uint32_t bmask = (1u << nbits) - 1u;
+      const uint32_t pmask = pass == 0 ? 0u : (0xffffffffu << (shift + nbits));
+      uint32_t* hb = hist + (pass & 1) * T * kHistWords;
+      for (int i = tid; i < T * kHistWords; i += kThreads) hb[i] = 0u;
+      __syncthreads();
+#pragma unroll 1
+      for (int tt = 0; tt < T; ++tt) {
+        if (!ctl->radix[tt]) continue;
+        const uint32_t pref = ctl->prefix[tt];
+        const uint32_t* sc = scores + tt * p.chunk;
+        uint32_t* h = hb + tt * kHistWords;
+        for (int e = tid; e < nscan; e += kThreads) {
+          const uint32_t u = sc[e];
+          if (u != 0u && (u & pmask) == pref) {
+            const uint32_t bin = (u >> shift) & bmask;
+            atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
+          }
+        }
+      }
+      cluster_sync();
+#pragma unroll 1
+      for (int tt = 0; tt < T; ++tt) {
+        if (!ctl->radix[tt]) continue;  // uniform over the block
+        uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        const uint32_t* h = hb + tt * kHistWords + 4 * tid;
+        for (int r = 0; r < p.C; ++r) {
+          const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
+          cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
+          cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
+          cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
+          cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
+        }
+        uint32_t sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sum += cnt[k];
+        if (tid == 0) {  // defaults, overwritten by the one thread whose bins hold the K-th key
+          ctl->found_bin[tt] = 0;
+          ctl->found_need[tt] = 1;
+        }
+        const uint32_t above = block_excl_suffix(sum, ctl->scan);
+        const uint32_t need = (uint32_t)ctl->need[tt];
+        uint32_t run = above;
+#pragma unroll
+        for (int k = 7; k >= 0; --k) {
+          if (run < need && run + cnt[k] >= need) {
+            ctl->found_bin[tt] = 8 * tid + k;
+            ctl->found_need[tt] = (int)(need - run);
+          }
+          run += cnt[k];
+        }
+        __syncthreads();
+        if (tid == 0) {
+          ctl->prefix[tt] |= (uint32_t)ctl->found_bin[tt] << shift;
+          ctl->need[tt] = ctl->found_need[tt];
+        }
+        __syncthreads();
+      }
+    }
+  }
+
+  // per-CTA counts above / at the threshold
+#pragma unroll 1
+  for (int tt = 0; tt < T; ++tt) {
+    const uint32_t thr = ctl->radix[tt] ? ctl->prefix[tt] : 0u;
+    const uint32_t* sc = scores + tt * p.chunk;
+    uint32_t gt = 0, eq = 0;
+    for (int e = tid; e < nscan; e += kThreads) {
+      const uint32_t u = sc[e];
+      gt += u > thr;
+      eq += (u == thr && u != 0u);
+    }
+    const uint32_t gsum = block_excl_suffix(gt, ctl->scan) + gt;  // thread 0 gets the total
+    const uint32_t esum = block_excl_suffix(eq, ctl->scan) + eq;
+    if (tid == 0) {
+      ctl->cnt_gt[tt] = (int)gsum;
+      ctl->cnt_eq[tt] = (int)esum;
+    }
+  }
+  cluster_sync();
+  if (tid < T) {
+    const int tt = tid;
+    const int need_eq = ctl->radix[tt] ? ctl->need[tt] : 0;
+    int eq_before = 0, off = 0, my_quota = 0;
+    for (int r = 0; r < p.C; ++r) {
+      const int gt_r = (int)ld_cluster_u32(map_cluster(&ctl->cnt_gt[tt], (uint32_t)r));
+      const int eq_r = (int)ld_cluster_u32(map_cluster(&ctl->cnt_eq[tt], (uint32_t)r));
+      const int quota_r = max(0, min(eq_r, need_eq - eq_before));
+      if (r < rank) off += gt_r + quota_r;
+      if (r == rank) my_quota = quota_r;
+      eq_before += eq_r;
+    }
+    ctl->offset[tt] = off;
+    ctl->quota[tt] = my_quota;
+  }
+  __syncthreads();
+
+  // ascending-position compaction of the selected positions
+#pragma unroll 1
+  for (int tt = 0; tt < nt; ++tt) {
+    const uint32_t thr = ctl->radix[tt] ? ctl->prefix[tt] : 0u;
+    const uint32_t quota = (uint32_t)ctl->quota[tt];
+    const int need_total = ctl->need_total[tt];
+    int* out = p.out_idx + (size_t)(t0 + tt) * p.K;
+    uint32_t eq_run = 0, sel_run = (uint32_t)ctl->offset[tt];
+    const uint32_t* sc = scores + tt * p.chunk;
+    for (int e0 = 0; e0 < nscan; e0 += kThreads) {
+      const int e = e0 + tid;
+      const uint32_t u = e < nscan ? sc[e] : 0u;
+      const bool f_eq = ctl->radix[tt] && u == thr && u != 0u;
+      uint32_t eq_pre, dummy, eq_tot, dummy_tot;
+      block_excl_flags(f_eq, false, ctl->scan, eq_pre, dummy, eq_tot, dummy_tot);
+      const bool take = (u > thr) || (f_eq && eq_run + eq_pre < quota);
+      uint32_t sel_pre, d2, sel_tot, d2t;
+      block_excl_flags(take, false, ctl->scan, sel_pre, d2, sel_tot, d2t);
+      if (take) {
+        const uint32_t slot = sel_run + sel_pre;
+        if ((int)slot < need_total)
+          out[slot] = lo + e;
+        else
+          report(p.status, kStatusDeviceCheck);
+      }
+      eq_run += eq_tot;
+      sel_run += sel_tot;
+    }
+    if (rank == 0) {
+      for (int r = need_total + tid; r < p.K; r += kThreads) out[r] = -1;
+      if (tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_total;
+    }
+  }
+  // peers may still be reading this CTA's counters
+  cluster_sync();
+}
+
+// ---------------------------------------------------------------- host side
+
+static bool use_cuda_core_scores() {
+  const char* e = std::getenv("DSA_LI_CUDA_CORE_SCORES");
+  return e && e[0] == '1';
+}
+
+template <int D_I, bool FP8, int H_I, int T>
+static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::string& err) {
+  using CF = Cfg<D_I, FP8, H_I, T>;
+  DeviceInfo dev;
+  if (!device_info(dev, err)) return DSA_ERR_CUDA;
+  const int groups = (a.max_q_per_seq + T - 1) / T;
+  const int maxL = std::max(a.max_seq_len, 1);
+
+  // Pick ring depth, cluster size and chunk: fewest estimated tile-rounds over the SMs.
+  int best_ns = 0, best_c = 0, best_chunk = 0, best_smem = 0;
+  double best_est = 1e300;
+  for (int ns = 4; ns >= 2; --ns) {
+    for (int c = 1; c <= kMaxCluster; ++c) {
+      const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
+      if (chunk > 65535) continue;  // 16-bit histogram counters
+      if ((long long)chunk * c < maxL) continue;
+      const Layout lay(ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
+      const int smem = lay.total + 1024;
+      if (smem > dev.smem_optin) continue;
+      // Model: every CTA streams chunk/128 tiles plus a fixed select overhead; the SM with the
+      // most CTAs sets the time; using few SMs is penalised (one SM cannot pull its share of
+      // HBM bandwidth alone); a 2-deep ring hides less latency.
+      const long long ctas = (long long)c * a.B * groups;
+      const long long per_sm = (ctas + dev.sm_count - 1) / dev.sm_count;
+      const double fill = std::max(1.0, 0.6 * dev.sm_count / (double)ctas);
+      const double est = (double)per_sm * (chunk / kTileKeys + 4) * fill * (ns >= 3 ? 1.0 : 1.15);
+      if (est < best_est - 1e-9) {
+        best_est = est;
+        best_ns = ns;
+        best_c = c;
+        best_chunk = chunk;
+        best_smem = smem;
+      }
+    }
+  }
+  if (!best_c) {
+    err = "li_topk: no (ring depth, cluster size) fits shared memory for max_seq_len " +
+          std::to_string(a.max_seq_len);
+    return DSA_ERR_UNSUPPORTED;
+  }
+  if (const char* e = std::getenv("DSA_LI_CLUSTER")) {  // tuning override
+    const int c = std::atoi(e);
+    if (c >= 1 && c <= kMaxCluster) {
+      const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
+      const Layout lay(best_ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
+      if (lay.total + 1024 <= dev.smem_optin && chunk <= 65535) {
+        best_c = c;
+        best_chunk = chunk;
+        best_smem = lay.total + 1024;
+      }
+    }
+  }
+
+  CUtensorMap tm_k, tm_q;
+  const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_tmap_2d(&tm_k, dt, a.k_pool, D_I, (uint64_t)a.num_pages * 64, CF::kRowBytes,
+                      128 / CF::kElt, 64, CU_TENSOR_MAP_SWIZZLE_128B, err))
+    return DSA_ERR_CUDA;
+  if (!encode_tmap_2d(&tm_q, dt, a.q, D_I, (uint64_t)a.n_q * H_I, CF::kRowBytes, 128 / CF::kElt,
+                      CF::kNCol, CU_TENSOR_MAP_SWIZZLE_128B, err))
+    return DSA_ERR_CUDA;
+
+  Params p;
+  p.B = a.B;
+  p.n_q = a.n_q;
+  p.K = a.K;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
+  p.groups = groups;
+  p.chunk = best_chunk;
+  p.C = best_c;
+  p.nstage = best_ns;
+  p.w = a.w;
+  p.q_scale = a.q_scale;
+  p.k_scale = a.k_scale;
+  p.page_table = a.page_table;
+  p.seq_lens = a.seq_lens;
+  p.q_start = a.q_start;
+  p.out_idx = a.out_idx;
+  p.out_cnt = a.out_cnt;
+  p.status = a.status;
+  p.q = a.q;
+  p.k_pool = a.k_pool;
+
+  const bool simple = use_cuda_core_scores();
+  auto kern = simple ? li_topk_kernel<D_I, FP8, H_I, T, false> : li_topk_kernel<D_I, FP8, H_I, T, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, best_smem);
+  if (e != cudaSuccess) return cuda_fail(e, "li_topk: set shared memory size", err);
+  if (best_c > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "li_topk: allow cluster > 8", err);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(best_c * a.B * groups));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)best_smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)best_c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (std::getenv("DSA_VERBOSE"))
+    std::fprintf(stderr, "[dsa] li_topk D_I=%d fp8=%d H_I=%d T=%d cluster=%d chunk=%d stages=%d smem=%d grid=%u\n",
+                 D_I, (int)FP8, H_I, T, best_c, best_chunk, best_ns, best_smem, cfg.gridDim.x);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_q, p);
+  if (e != cudaSuccess) return cuda_fail(e, "li_topk: launch", err);
+  return DSA_OK;
+}
+
+}  // namespace li
+
+dsa_status launch_li_topk(const dsa_li_args& a, cudaStream_t stream, std::string& err) {
+  const int T = a.max_q_per_seq <= 1 ? 1 : (a.max_q_per_seq <= 2 ? 2 : 4);
+  const bool fp8 = a.dtype == DSA_FP8_E4M3;
+  if (a.H_I == 64 && a.d_I == 128) {
+    if (fp8) {
+      if (T == 1) return li::launch_impl<128, true, 64, 1>(a, stream, err);
+      if (T == 2) return li::launch_impl<128, true, 64, 2>(a, stream, err);
+      return li::launch_impl<128, true, 64, 4>(a, stream, err);
+    }
+    if (T == 1) return li::launch_impl<128, false, 64, 1>(a, stream, err);
+    if (T == 2) return li::launch_impl<128, false, 64, 2>(a, stream, err);
+    return li::launch_impl<128, false, 64, 4>(a, stream, err);
+  }
+  if (a.H_I == 8 && a.d_I == 64 && !fp8) {
+    if (T == 1) return li::launch_impl<64, false, 8, 1>(a, stream, err);
+    if (T == 2) return li::launch_impl<64, false, 8, 2>(a, stream, err);
+    return li::launch_impl<64, false, 8, 4>(a, stream, err);
+  }
+  err = "li_topk: unsupported (H_I, d_I, dtype) = (" + std::to_string(a.H_I) + ", " +
+        std::to_string(a.d_I) + ", " + (fp8 ? "fp8" : "bf16") + ")";
+  return DSA_ERR_UNSUPPORTED;
+}
+
+}  // namespace dsa

@@ -1,0 +1,194 @@
+/*
+ * dsa.h -- C ABI of the DSA (Dynamic Sparse Attention) hot path for GB300 (sm_103a).
+ *
+ * The path, as the public pages on Kimi K3.1 Pro inference describe it:
+ *   1. Lightning Indexer: score the query against every cached key with per-head weights
+ *      ("Inference Optimization for Kimi K3.1 Pro: Decoding Architecture Evolution and Systems
+ *      Engineering Practices", section 1, DSA step 1; "Day0 Inference Adaptation for Next-Gen
+ *      LLMs ... CANN", section 3.1),
+ *   2. keep the top-K positions, fused with scoring so that no score reaches global memory
+ *      (first page, section 2 "Operator-Level Deep Fusion"),
+ *   3. Sparse Flash Attention over only those positions of the paged MLA latent cache, blockwise
+ *      with a cross-block softmax reduction ("Optimizing Kimi K3.1 Pro Sparse Attention
+ *      Inference ...", section "Inheritance and Extension of Core Operators").
+ *
+ * Conventions shared by every call:
+ *   - Every pointer in an args struct is a DEVICE pointer owned by the caller.  The library never
+ *     allocates, never frees, never synchronises and keeps no pointer after it returns.  Work is
+ *     enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and runs
+ *     asynchronously.
+ *   - Synchronous errors (bad shape, null pointer, unsupported specialisation) are returned
+ *     before anything is launched; dsa_last_error() then holds a one-line reason for the calling
+ *     thread.  A failed launch returns DSA_ERR_CUDA.
+ *   - Device-side checks (an index, length or page id out of range, a bounded wait that ran out)
+ *     never trap: the kernel skips the offending work and stores a DSA_ERR_* code into *status
+ *     (when status is not NULL; first error wins).  The caller reads it after synchronising.
+ *   - Caches are paged with `page_size` rows per page.  Logical position j of sequence b lives at
+ *     physical row page_table[b * max_pages + j / page_size] * page_size + j % page_size.
+ *   - Query tokens are packed over sequences: the tokens of sequence b are q_start[b] ..
+ *     q_start[b+1]-1; they are the last n_b = q_start[b+1]-q_start[b] positions of the sequence,
+ *     so token i of sequence b sits at position seq_lens[b] - n_b + i (the keys and latent rows of
+ *     the new tokens are already in the caches) and sees positions 0 .. that position.
+ *   - Indices are LOGICAL positions, so results do not depend on where pages are placed.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dsa_stream_t;
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,  /* null pointer, negative or inconsistent size                    */
+  DSA_ERR_UNSUPPORTED = 2,  /* valid, but no compiled specialisation covers it                */
+  DSA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a launch failed                  */
+  DSA_ERR_DEVICE_CHECK = 4, /* (in *status) a device-side range check failed                  */
+  DSA_ERR_TIMEOUT = 5       /* (in *status) a bounded device-side wait gave up                */
+} dsa_status;
+
+typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1 } dsa_dtype;
+
+/* Human-readable name of a status code (static storage). */
+const char* dsa_status_string(dsa_status s);
+
+/* Reason for the last synchronous error returned on the calling thread ("" if none). */
+const char* dsa_last_error(void);
+
+/* DSA_ABI_VERSION of the built library. */
+int dsa_abi_version(void);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Lightning Indexer + top-K                                                                   */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * For every query token t (at position p):
+ *   s(t, j) = sum_{h < H_I} w[t][h] * max(0, q[t][h][:] . k[j][:])      for 0 <= j <= p,
+ * with one index key row k[j] (d_I wide) per position, shared by all index heads; in FP8 mode
+ * q[t][h][:] = q8 * q_scale[t][h] and k[j][:] = k8 * k_scale[row(j)].  The selected set is the
+ * first min(K, p+1) positions in the order (score descending, position ascending) -- ties go to
+ * the lower position, and -0.0 equals +0.0.  Scores never leave the chip.
+ *
+ * Supported: page_size 64; (H_I, d_I) in {(8, 64), (64, 128)}; dtype BF16 or FP8_E4M3 (d_I 128);
+ * 1 <= K <= 2048; max_seq_len <= 131072; any number of tokens per sequence (decode, speculative
+ * multi-token decode, chunked prefill).
+ */
+typedef struct {
+  int B;            /* sequences                                                         */
+  int n_q;          /* query tokens over all sequences (= q_start[B])                    */
+  int H_I, d_I;     /* index heads, index head dim                                        */
+  int K;            /* top-K                                                              */
+  int page_size;    /* rows per page (64)                                                 */
+  int max_pages;    /* row stride of page_table                                           */
+  int num_pages;    /* pages in k_pool (device check on every page id)                     */
+  int max_seq_len;  /* host-known upper bound of seq_lens[] (sizes the launch)            */
+  int max_q_per_seq;/* host-known upper bound of q_start[b+1]-q_start[b]                  */
+  dsa_dtype dtype;
+  const void* q;          /* [n_q][H_I][d_I]   bf16 | e4m3                                */
+  const float* q_scale;   /* [n_q][H_I] fp32, FP8 only (per-token scales: replicate)      */
+  const float* w;         /* [n_q][H_I] fp32 head weights                                 */
+  const void* k_pool;     /* [num_pages][page_size][d_I]  bf16 | e4m3                     */
+  const float* k_scale;   /* [num_pages][page_size] fp32, FP8 only                        */
+  const int32_t* page_table; /* [B][max_pages] physical page ids                          */
+  const int32_t* seq_lens;   /* [B] positions, new tokens included                        */
+  const int32_t* q_start;    /* [B+1] prefix offsets of the query tokens                  */
+  int32_t* out_idx;       /* [n_q][K] selected positions, ascending, then -1 padding      */
+  int32_t* out_cnt;       /* [n_q] number selected = min(K, p+1), or NULL                 */
+  int32_t* status;        /* device int32 error word, or NULL                             */
+} dsa_li_args;
+
+dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Sparse Flash Attention                                                                      */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * For every query token t and head h, over the index set S_t = {idx[t][r] : idx[t][r] >= 0}:
+ *   z_j = softmax_scale * q[t][h][0:d_qk] . kv[j][0:d_qk]
+ *   out[t][h][:] = sum_j exp(z_j - m) kv[j][0:d_v] / sum_j exp(z_j - m),   m = max_j z_j
+ *   lse[t][h]    = m + ln(sum_j exp(z_j - m))
+ * The value is the leading d_v columns of the same latent row (MLA), so each selected row is
+ * read once.  An empty set gives out = 0 and lse = -inf.  An index >= seq_lens[b] or < -1 is a
+ * device check failure: the row is skipped and *status set.
+ *
+ * dsa_sfa_decode targets few tokens per sequence (splits each token's K rows over several CTAs
+ * and merges the partial softmax states in `workspace`); dsa_sfa_prefill targets many tokens
+ * per sequence (one token per CTA pair, no workspace).  Both give the same result up to fp32
+ * rounding.
+ *
+ * Supported: page_size 64; d_qk 576; d_v 512; H in {16, 128} (decode) and 128 (prefill);
+ * 1 <= K <= 2048; bf16 q/kv/out.
+ */
+typedef struct {
+  int B, n_q;
+  int H;              /* query heads                                                     */
+  int d_qk, d_v;      /* 576, 512                                                        */
+  int K;              /* row stride of idx                                               */
+  int page_size, max_pages, num_pages;
+  int max_seq_len, max_q_per_seq;
+  float softmax_scale;
+  const void* q;             /* [n_q][H][d_qk] bf16                                      */
+  const void* kv_pool;       /* [num_pages][page_size][d_qk] bf16                        */
+  const int32_t* page_table; /* [B][max_pages]                                           */
+  const int32_t* seq_lens;   /* [B]                                                      */
+  const int32_t* q_start;    /* [B+1]                                                    */
+  const int32_t* idx;        /* [n_q][K] logical positions, -1 = empty slot              */
+  void* out;                 /* [n_q][H][d_v] bf16                                       */
+  float* lse;                /* [n_q][H] fp32, or NULL                                   */
+  int32_t* status;           /* device int32 error word, or NULL                         */
+  void* workspace;           /* device scratch of dsa_sfa_workspace_bytes(), 256-B aligned */
+  size_t workspace_bytes;
+} dsa_sfa_args;
+
+/* Scratch that dsa_sfa_decode needs for these arguments (0 if none).  Host only, no CUDA. */
+size_t dsa_sfa_workspace_bytes(const dsa_sfa_args* args);
+
+dsa_status dsa_sfa_decode(const dsa_sfa_args* args, dsa_stream_t stream);
+dsa_status dsa_sfa_prefill(const dsa_sfa_args* args, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Cache layout and page-table helpers                                                         */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Bytes of one page of `rows` rows of `dim` elements of `dtype` (0 on invalid input). */
+size_t dsa_page_bytes(dsa_dtype dtype, int rows, int dim);
+
+/*
+ * Host-side check of a page table (host pointers): for every sequence b, the pages
+ * 0 .. ceil(seq_lens[b]/page_size)-1 hold ids in [0, num_pages), and (if require_unique) no id
+ * is used twice over the whole table.  Entries past a sequence's last page are ignored.
+ * Returns DSA_OK or DSA_ERR_INVALID_ARG (reason in dsa_last_error()).
+ */
+dsa_status dsa_page_table_validate(const int32_t* page_table_host, int B, int max_pages,
+                                   const int32_t* seq_lens_host, int page_size, int num_pages,
+                                   int require_unique);
+
+/*
+ * Scatter n_rows new cache rows into a paged pool (device pointers):
+ *   pool[page_table[seq[r]][pos[r] / page_size]][pos[r] % page_size][:] = rows[r][:]
+ * and, when row_scales is not NULL, scale_pool[same page][same slot] = row_scales[r] (the
+ * per-row fp32 scale of an FP8 key cache).  elem_bytes is 2 (bf16) or 1 (e4m3); dim*elem_bytes
+ * must be a multiple of 16.  Out-of-range seq/pos/page entries are skipped and flagged in
+ * *status.
+ */
+dsa_status dsa_cache_write(void* pool, float* scale_pool, int num_pages, int page_size, int dim,
+                           int elem_bytes, const int32_t* page_table, int max_pages, int B,
+                           const int32_t* seq, const int32_t* pos, const void* rows,
+                           const float* row_scales, int n_rows, int32_t* status,
+                           dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

@@ -1,0 +1,133 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol include/dsa.h declares,
+and rejects bad arguments on the host before touching CUDA (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import dsa_sparse_attention_li_gb300 as dsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = dsa.load()
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(names) == sorted(dsa.SYMBOLS)
+
+
+def test_abi_version_and_status_strings():
+    lib = dsa.load()
+    assert lib.dsa_abi_version() == 1
+    assert dsa.status_string(0) == "DSA_OK"
+    assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
+    assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"
+
+
+def test_struct_layouts_match_header():
+    """ctypes mirrors of the argument structs have the C sizes (x86_64 / aarch64 LP64)."""
+    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 11 * 8
+    assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8
+
+
+def test_page_bytes():
+    assert dsa.page_bytes(dsa.DSA_BF16, 64, 576) == 64 * 576 * 2
+    assert dsa.page_bytes(dsa.DSA_FP8_E4M3, 64, 128) == 64 * 128
+    assert dsa.page_bytes(dsa.DSA_BF16, -1, 4) == 0
+
+
+def test_page_table_validate():
+    pt = torch.tensor([[3, 1, 0], [2, 0, 0]], dtype=torch.int32)
+    sl = torch.tensor([130, 64], dtype=torch.int32)
+    dsa.page_table_validate(pt, sl, 64, 4, require_unique=True)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.page_table_validate(pt, sl, 64, 3)          # page 3 out of range
+    assert "out of" in str(e.value)
+    with pytest.raises(dsa.DsaError):
+        dsa.page_table_validate(torch.tensor([[1, 1, 0], [2, 0, 0]], dtype=torch.int32), sl, 64, 4,
+                                require_unique=True)    # page 1 used twice
+    with pytest.raises(dsa.DsaError):
+        dsa.page_table_validate(pt, torch.tensor([200, 1], dtype=torch.int32), 64, 4)  # > max_pages
+
+
+def _li(**over):
+    a = dsa.LiArgs()
+    a.B, a.n_q, a.H_I, a.d_I, a.K, a.page_size, a.max_pages, a.num_pages = 1, 1, 64, 128, 2048, 64, 8, 8
+    a.max_seq_len, a.max_q_per_seq, a.dtype = 512, 1, dsa.DSA_BF16
+    for n in ("q", "w", "k_pool", "page_table", "seq_lens", "q_start", "out_idx"):
+        setattr(a, n, 4096)  # fake, aligned, never dereferenced on these error paths
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"K": 0}, dsa.DSA_ERR_INVALID_ARG),
+    ({"B": 0}, dsa.DSA_ERR_INVALID_ARG),
+    ({"dtype": 7}, dsa.DSA_ERR_INVALID_ARG),
+    ({"q": None}, dsa.DSA_ERR_INVALID_ARG),
+    ({"dtype": dsa.DSA_FP8_E4M3}, dsa.DSA_ERR_INVALID_ARG),   # no scales
+    ({"max_seq_len": 8 * 64 + 1}, dsa.DSA_ERR_INVALID_ARG),
+    ({"q": 4097}, dsa.DSA_ERR_INVALID_ARG),                    # misaligned
+    ({"K": 4096}, dsa.DSA_ERR_UNSUPPORTED),
+    ({"page_size": 32, "max_pages": 16}, dsa.DSA_ERR_UNSUPPORTED),
+])
+def test_li_topk_host_validation(over, code):
+    lib = dsa.load()
+    rc = lib.dsa_li_topk(ctypes.byref(_li(**over)), None)
+    assert rc == code, dsa.last_error()
+    assert dsa.last_error()
+
+
+def test_li_topk_null_args_and_empty_batch():
+    lib = dsa.load()
+    assert lib.dsa_li_topk(None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_li_topk(ctypes.byref(_li(n_q=0)), None) == dsa.DSA_OK
+
+
+def _sfa(**over):
+    a = dsa.SfaArgs()
+    a.B, a.n_q, a.H, a.d_qk, a.d_v, a.K, a.page_size, a.max_pages, a.num_pages = 1, 1, 128, 576, 512, 2048, 64, 8, 8
+    a.max_seq_len, a.max_q_per_seq, a.softmax_scale = 512, 1, 1 / 24
+    for n in ("q", "kv_pool", "page_table", "seq_lens", "q_start", "idx", "out"):
+        setattr(a, n, 4096)
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"H": 0}, dsa.DSA_ERR_INVALID_ARG),
+    ({"softmax_scale": 0.0}, dsa.DSA_ERR_INVALID_ARG),
+    ({"softmax_scale": float("nan")}, dsa.DSA_ERR_INVALID_ARG),
+    ({"idx": None}, dsa.DSA_ERR_INVALID_ARG),
+    ({"out": 4100}, dsa.DSA_ERR_INVALID_ARG),
+    ({"d_qk": 512}, dsa.DSA_ERR_UNSUPPORTED),
+    ({"H": 256}, dsa.DSA_ERR_UNSUPPORTED),
+    ({"K": 4096}, dsa.DSA_ERR_UNSUPPORTED),
+])
+@pytest.mark.parametrize("entry", ["dsa_sfa_decode", "dsa_sfa_prefill"])
+def test_sfa_host_validation(over, code, entry):
+    lib = dsa.load()
+    rc = getattr(lib, entry)(ctypes.byref(_sfa(**over)), None)
+    assert rc == code, dsa.last_error()
+
+
+def test_cache_write_host_validation():
+    lib = dsa.load()
+    P = 4096
+    assert lib.dsa_cache_write(P, None, 4, 64, 576, 3, P, 4, 1, P, P, P, None, 1, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_write(P, None, 4, 64, 4, 2, P, 4, 1, P, P, P, None, 1, None, None) == dsa.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_cache_write(P, P, 4, 64, 576, 2, P, 4, 1, P, P, P, None, 1, None, None) == dsa.DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_write(P, None, 4, 64, 576, 2, P, 4, 1, P, P, P, None, 0, None, None) == dsa.DSA_OK

@@ -1,0 +1,180 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle on seeded inputs.
+
+Small cases span several 128-key tiles, several CTAs of a cluster and ragged tails; the five
+full-size workloads run in the launch configuration the benchmark times and are checked on
+sampled tokens.  Index sets are bit-exact on the integer-valued configs; elsewhere differences
+must be certified near-ties.  Attention outputs stay within max-abs 2e-2 / mean-rel 5e-3 (bf16)
+of the fp64 oracle on the GPU's own index sets, and within 5e-2 / 1e-2 end to end on the FP8
+indexer path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dsa_inputs as di
+import dsa_sparse_attention_li_gb300 as dsa
+from parity import (BF16_TOL, FP8_TOL, check_indices, check_sfa, integer_fp8, run_gpu,
+                    sample_tokens, sfa_errors)
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(name, **over):
+    wl = di.small(name, **over)
+    inp_cpu = di.generate(wl)
+    return inp_cpu, di.to_device(inp_cpu, "cuda")
+
+
+# ------------------------------------------------------------------ indexer + attention, small
+
+@pytest.mark.parametrize("lens,new", [([4096], [1]), ([300, 4096, 1000], [1, 2, 3]),
+                                      ([70, 129, 2500], [1, 1, 1]), ([63], [1])])
+def test_integer_config_bit_exact(cuda_lib, lens, new):
+    inp_cpu, inp = _small("decode_int_4k", seq_lens=lens, n_new=new)
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    n_exact, ties = check_indices(inp_cpu, g, toks, exact=True)
+    assert n_exact == len(toks)
+    check_sfa(inp_cpu, g, toks)
+
+
+@pytest.mark.parametrize("lens,new", [([5000, 2100, 777], [1, 1, 1]), ([9000, 3000], [2, 2]),
+                                      ([2047, 2048, 2049], [1, 2, 1])])
+def test_bf16_indexer_and_attention_small(cuda_lib, lens, new):
+    inp_cpu, inp = _small("decode_32k", seq_lens=lens, n_new=new)
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    check_indices(inp_cpu, g, toks, exact=False)
+    check_sfa(inp_cpu, g, toks)
+
+
+def test_fp8_integer_unit_case_bit_exact(cuda_lib):
+    inp_cpu, _ = _small("decode_32k_fp8", seq_lens=[6000, 2500, 300], n_new=[1, 2, 1])
+    inp_cpu = integer_fp8(inp_cpu, seed=3)
+    inp = di.to_device(inp_cpu, "cuda")
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    n_exact, _ = check_indices(inp_cpu, g, toks, exact=True)
+    assert n_exact == len(toks)
+
+
+def test_fp8_normal_small(cuda_lib):
+    inp_cpu, inp = _small("decode_32k_fp8", seq_lens=[7000, 3100], n_new=[1, 2])
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    check_indices(inp_cpu, g, toks, exact=False)
+    check_sfa(inp_cpu, g, toks)
+
+
+def test_prefill_small(cuda_lib):
+    inp_cpu, inp = _small("prefill_64k", seq_lens=[3000], n_new=[300], K=256)
+    g = run_gpu(inp, prefill=True)
+    assert g["status"] == 0
+    toks = sample_tokens(inp_cpu["wl"], 12, seed=1)
+    check_indices(inp_cpu, g, toks, exact=False)
+    check_sfa(inp_cpu, g, toks)
+
+
+def test_decode_and_prefill_attention_agree(cuda_lib):
+    inp_cpu, inp = _small("decode_32k", seq_lens=[4000, 5000], n_new=[1, 1])
+    a = run_gpu(inp, prefill=False)
+    b = run_gpu(inp, prefill=True)
+    assert np.array_equal(a["idx"], b["idx"])
+    d = (a["out"] - b["out"]).abs().max().item()
+    assert d <= 2e-2, d
+
+
+def test_k_covers_context_selects_everything(cuda_lib):
+    inp_cpu, inp = _small("decode_32k", seq_lens=[1500, 64, 2048], n_new=[1, 2, 1])
+    g = run_gpu(inp)
+    pos = di.token_positions(inp_cpu["wl"])
+    for t, p in enumerate(pos):
+        assert g["idx"][t].tolist() == list(range(p + 1)) + [-1] * (2048 - p - 1)
+    check_sfa(inp_cpu, g, list(range(len(pos))))
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+def test_page_permutation_invariance_and_determinism(cuda_lib):
+    inp_cpu, inp = _small("decode_32k", seq_lens=[6000, 3000], n_new=[1, 2])
+    a = run_gpu(inp)
+    a2 = run_gpu(inp)
+    assert np.array_equal(a["idx"], a2["idx"]) and torch.equal(a["out"], a2["out"])
+    inp_r = di.to_device(di.repage(inp_cpu, seed=77), "cuda")
+    b = run_gpu(inp_r)
+    assert np.array_equal(a["idx"], b["idx"])
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["lse"], b["lse"])
+
+
+def test_bad_page_id_sets_status_without_fault(cuda_lib):
+    inp_cpu, inp = _small("decode_32k", seq_lens=[3000], n_new=[1])
+    pt = inp["pt_k"].clone()
+    pt[0, 5] = inp["k_pool"].shape[0] + 100
+    inp = dict(inp, pt_k=pt)
+    g = run_gpu(inp)
+    assert g["status"] == dsa.DSA_ERR_DEVICE_CHECK
+    torch.cuda.synchronize()  # the context is still usable
+
+
+def test_cache_write_roundtrip(cuda_lib):
+    inp_cpu, inp = _small("decode_32k", seq_lens=[200, 100], n_new=[1, 1])
+    pool = torch.zeros_like(inp["kv_pool"])
+    seq = torch.tensor([0, 0, 1, 1], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([0, 199, 5, 99], dtype=torch.int32, device="cuda")
+    rows = torch.randn(4, 576, device="cuda").to(torch.bfloat16)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dsa.cache_write(pool, inp["pt_kv"], seq, pos, rows, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    pt = inp["pt_kv"].cpu()
+    for r in range(4):
+        b, j = int(seq[r]), int(pos[r])
+        assert torch.equal(pool[int(pt[b, j // 64]), j % 64], rows[r])
+
+
+def test_cuda_graph_replay_matches_eager(cuda_lib):
+    inp_cpu, inp = _small("decode_32k", seq_lens=[5000, 4000], n_new=[1, 1])
+    eager = run_gpu(inp)
+    wl = inp["wl"]
+    idx = torch.empty((wl.n_q, wl.K), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((wl.n_q,), dtype=torch.int32, device="cuda")
+    out = torch.empty((wl.n_q, wl.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.n_q, wl.H), dtype=torch.float32, device="cuda")
+    ws = dsa.new_workspace(dsa.sfa_workspace_bytes(inp["q_sfa"], idx), "cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dsa.decode_step(inp, idx=idx, cnt=cnt, out=out, lse=lse, workspace=ws)  # warm-up
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        dsa.decode_step(inp, idx=idx, cnt=cnt, out=out, lse=lse, workspace=ws)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), eager["idx"])
+    assert torch.equal(out.float().cpu(), eager["out"])
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+FULL = [("decode_int_4k", True, BF16_TOL), ("decode_32k", False, BF16_TOL),
+        ("decode_32k_fp8", False, FP8_TOL), ("specdec_ragged", False, BF16_TOL),
+        ("prefill_64k", False, BF16_TOL)]
+
+
+@pytest.mark.parametrize("name,exact,tol", FULL, ids=[f[0] for f in FULL])
+def test_full_size_workload_sampled(cuda_lib, name, exact, tol):
+    wl = di.preset(name)
+    inp = di.generate(wl, device="cuda")
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    inp_cpu = di.to_device(inp, "cpu")
+    toks = sample_tokens(wl, 4 if wl.n_q > 4 else wl.n_q, seed=11)
+    n_exact, ties = check_indices(inp_cpu, g, toks, exact=exact)
+    check_sfa(inp_cpu, g, toks)            # attention alone, bf16 tolerance
+    if not exact:
+        print("%s: %d/%d index rows exact, near-ties %s" % (name, n_exact, len(toks), ties))
