@@ -17,15 +17,20 @@
 //                    warps 4..7 (one TMEM lane = one key per thread) apply ReLU, the head weights
 //                    and the head sum, mask by causality and length, and store an order-preserving
 //                    32-bit key of each score in shared memory;
-//   select phase     three radix passes (11/11/10 bits) build per-CTA histograms whose cluster
-//                    total is read over distributed shared memory; every CTA derives the same
-//                    K-th key and the number of ties to take; per-CTA counts give each CTA its
-//                    output offset and tie quota (ties go to the lowest positions, CTAs own
-//                    ascending position ranges), and a ballot compaction writes the positions in
-//                    ascending order.
+//   select phase     three radix passes (11/11/10 bits; the first histogram is built by the
+//                    epilogue while keys stream) give per-CTA histograms whose cluster total is
+//                    read over distributed shared memory; every CTA derives the same K-th key
+//                    and the number of ties to take; per-warp counts give each warp its output
+//                    offset and tie quota (ties go to the lowest positions; CTAs and warps own
+//                    ascending position ranges), and a warp-ballot compaction writes the
+//                    positions in ascending order.
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "dsa_internal.h"
 #include "ptx.cuh"
@@ -107,6 +112,7 @@ struct Ctl {
   int cnt_gt[4], cnt_eq[4];  // this CTA's counts (read by the cluster)
   int offset[4], quota[4];
   int found_bin[4], found_need[4];
+  int wgt[4][8], weq[4][8];  // per-warp counts above / at the threshold
 };
 
 // ---- block-level scans over 256 threads ----
@@ -128,32 +134,6 @@ DSA_DEV uint32_t block_excl_suffix(uint32_t v, uint32_t* scratch) {
     if (w > warp) above += scratch[w];
   __syncthreads();
   return above + x - v;
-}
-
-// Exclusive prefix counts of two flags at once; totals returned through tot_a / tot_b.
-DSA_DEV void block_excl_flags(bool fa, bool fb, uint32_t* scratch, uint32_t& pa, uint32_t& pb,
-                              uint32_t& tot_a, uint32_t& tot_b) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t ma = __ballot_sync(0xffffffffu, fa), mb = __ballot_sync(0xffffffffu, fb);
-  const uint32_t lt = (1u << lane) - 1u;
-  if (lane == 0) scratch[warp] = (uint32_t)__popc(ma) | ((uint32_t)__popc(mb) << 16);
-  __syncthreads();
-  uint32_t ba = 0, bb = 0, ta = 0, tb = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) {
-    const uint32_t c = scratch[w];
-    if (w < warp) {
-      ba += c & 0xffffu;
-      bb += c >> 16;
-    }
-    ta += c & 0xffffu;
-    tb += c >> 16;
-  }
-  __syncthreads();
-  pa = ba + __popc(ma & lt);
-  pb = bb + __popc(mb & lt);
-  tot_a = ta;
-  tot_b = tb;
 }
 
 DSA_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -240,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pages[i] = id;
   }
+  for (int i = tid; i < T * kHistWords; i += kThreads) hist[i] = 0u;  // pass-0 histogram
   for (int i = tid; i < T * H_I; i += kThreads) {
     const int tt = i / H_I, h = i % H_I;
     float v = 0.f;
@@ -352,7 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (FP8) s *= ks;
           const bool valid = tt < nt && j < lo + p.chunk && j <= pos0 + tt;
-          if (j - lo < p.chunk) scores[tt * p.chunk + (j - lo)] = valid ? score_key(s) : 0u;
+          const uint32_t u = valid ? score_key(s) : 0u;
+          scores[tt * p.chunk + (j - lo)] = u;
+          if (valid) atomicAdd(&hist[tt * kHistWords + (u >> 22)], 1u << (((u >> 21) & 1u) * 16u));
         }
         tc_fence_before();
         mbar_arrive(&ctl->tempty[a]);
@@ -385,7 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (FP8) s *= ks;
         const bool valid = tt < nt && pg >= 0 && j <= pos0 + tt;
-        scores[tt * p.chunk + e] = valid ? score_key(s) : 0u;
+        const uint32_t u = valid ? score_key(s) : 0u;
+        scores[tt * p.chunk + e] = u;
+        if (valid) atomicAdd(&hist[tt * kHistWords + (u >> 22)], 1u << (((u >> 21) & 1u) * 16u));
       }
     }
   }
@@ -419,10 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bmask = (1u << nbits) - 1u;
       const uint32_t pmask = pass == 0 ? 0u : (0xffffffffu << (shift + nbits));
       uint32_t* hb = hist + (pass & 1) * T * kHistWords;
-      for (int i = tid; i < T * kHistWords; i += kThreads) hb[i] = 0u;
-      __syncthreads();
+      if (pass > 0) {  // pass 0 was built by the epilogue while the keys streamed
+        for (int i = tid; i < T * kHistWords; i += kThreads) hb[i] = 0u;
+        __syncthreads();
+      }
 #pragma unroll 1
-      for (int tt = 0; tt < T; ++tt) {
+      for (int tt = 0; tt < T && pass > 0; ++tt) {
         if (!ctl->radix[tt]) continue;
         const uint32_t pref = ctl->prefix[tt];
         const uint32_t* sc = scores + tt * p.chunk;
@@ -476,23 +463,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // per-CTA counts above / at the threshold
+  // Counts above / at the threshold.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of
+  // this CTA's positions, so the compaction below needs no block-wide barrier.
+  const int seg = ((nscan + kThreads / 32 - 1) / (kThreads / 32) + 31) / 32 * 32;
+  const int e_lo = warp * seg, e_hi = min(nscan, e_lo + seg);
 #pragma unroll 1
   for (int tt = 0; tt < T; ++tt) {
     const uint32_t thr = ctl->radix[tt] ? ctl->prefix[tt] : 0u;
     const uint32_t* sc = scores + tt * p.chunk;
     uint32_t gt = 0, eq = 0;
-    for (int e = tid; e < nscan; e += kThreads) {
+    for (int e = e_lo + lane; e < e_hi; e += 32) {
       const uint32_t u = sc[e];
       gt += u > thr;
       eq += (u == thr && u != 0u);
     }
-    const uint32_t gsum = block_excl_suffix(gt, ctl->scan) + gt;  // thread 0 gets the total
-    const uint32_t esum = block_excl_suffix(eq, ctl->scan) + eq;
-    if (tid == 0) {
-      ctl->cnt_gt[tt] = (int)gsum;
-      ctl->cnt_eq[tt] = (int)esum;
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if (lane == 0) {
+      ctl->wgt[tt][warp] = (int)gt;
+      ctl->weq[tt][warp] = (int)eq;
     }
+  }
+  __syncthreads();
+  if (tid < T) {
+    int g = 0, q = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      g += ctl->wgt[tid][w];
+      q += ctl->weq[tid][w];
+    }
+    ctl->cnt_gt[tid] = g;
+    ctl->cnt_eq[tid] = q;
   }
   cluster_sync();
   if (tid < T) {
@@ -512,33 +512,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  // ascending-position compaction of the selected positions
+  // ascending-position compaction: ties at the threshold go to the lowest positions
+  const uint32_t lt_mask = (1u << lane) - 1u;
 #pragma unroll 1
   for (int tt = 0; tt < nt; ++tt) {
-    const uint32_t thr = ctl->radix[tt] ? ctl->prefix[tt] : 0u;
-    const uint32_t quota = (uint32_t)ctl->quota[tt];
+    const bool radix = ctl->radix[tt] != 0;
+    const uint32_t thr = radix ? ctl->prefix[tt] : 0u;
     const int need_total = ctl->need_total[tt];
+    int eq_before = 0, off = ctl->offset[tt];
+    for (int w = 0; w < warp; ++w) {
+      const int ties_w = max(0, min(ctl->weq[tt][w], ctl->quota[tt] - eq_before));
+      off += ctl->wgt[tt][w] + ties_w;
+      eq_before += ctl->weq[tt][w];
+    }
+    const int my_ties = max(0, min(ctl->weq[tt][warp], ctl->quota[tt] - eq_before));
     int* out = p.out_idx + (size_t)(t0 + tt) * p.K;
-    uint32_t eq_run = 0, sel_run = (uint32_t)ctl->offset[tt];
     const uint32_t* sc = scores + tt * p.chunk;
-    for (int e0 = 0; e0 < nscan; e0 += kThreads) {
-      const int e = e0 + tid;
-      const uint32_t u = e < nscan ? sc[e] : 0u;
-      const bool f_eq = ctl->radix[tt] && u == thr && u != 0u;
-      uint32_t eq_pre, dummy, eq_tot, dummy_tot;
-      block_excl_flags(f_eq, false, ctl->scan, eq_pre, dummy, eq_tot, dummy_tot);
-      const bool take = (u > thr) || (f_eq && eq_run + eq_pre < quota);
-      uint32_t sel_pre, d2, sel_tot, d2t;
-      block_excl_flags(take, false, ctl->scan, sel_pre, d2, sel_tot, d2t);
+    int eq_run = 0, sel_run = off;
+    for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
+      const int e = e0 + lane;
+      const uint32_t u = e < e_hi ? sc[e] : 0u;
+      const bool f_eq = radix && u == thr && u != 0u;
+      const uint32_t meq = __ballot_sync(0xffffffffu, f_eq);
+      const bool take = (u > thr) || (f_eq && eq_run + __popc(meq & lt_mask) < my_ties);
+      const uint32_t mt = __ballot_sync(0xffffffffu, take);
       if (take) {
-        const uint32_t slot = sel_run + sel_pre;
-        if ((int)slot < need_total)
+        const int slot = sel_run + __popc(mt & lt_mask);
+        if (slot < need_total)
           out[slot] = lo + e;
         else
           report(p.status, kStatusDeviceCheck);
       }
-      eq_run += eq_tot;
-      sel_run += sel_tot;
+      eq_run += __popc(meq);
+      sel_run += __popc(mt);
     }
     if (rank == 0) {
       for (int r = need_total + tid; r < p.K; r += kThreads) out[r] = -1;
@@ -564,50 +570,80 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   const int groups = (a.max_q_per_seq + T - 1) / T;
   const int maxL = std::max(a.max_seq_len, 1);
 
-  // Pick ring depth, cluster size and chunk: fewest estimated tile-rounds over the SMs.
-  int best_ns = 0, best_c = 0, best_chunk = 0, best_smem = 0;
-  double best_est = 1e300;
-  for (int ns = 4; ns >= 2; --ns) {
-    for (int c = 1; c <= kMaxCluster; ++c) {
-      const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
-      if (chunk > 65535) continue;  // 16-bit histogram counters
-      if ((long long)chunk * c < maxL) continue;
-      const Layout lay(ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
-      const int smem = lay.total + 1024;
-      if (smem > dev.smem_optin) continue;
-      // Model: every CTA streams chunk/128 tiles plus a fixed select overhead; the SM with the
-      // most CTAs sets the time; using few SMs is penalised (one SM cannot pull its share of
-      // HBM bandwidth alone); a 2-deep ring hides less latency.
-      const long long ctas = (long long)c * a.B * groups;
-      const long long per_sm = (ctas + dev.sm_count - 1) / dev.sm_count;
-      const double fill = std::max(1.0, 0.6 * dev.sm_count / (double)ctas);
-      const double est = (double)per_sm * (chunk / kTileKeys + 4) * fill * (ns >= 3 ? 1.0 : 1.15);
-      if (est < best_est - 1e-9) {
-        best_est = est;
-        best_ns = ns;
-        best_c = c;
-        best_chunk = chunk;
-        best_smem = smem;
+  const bool simple = use_cuda_core_scores();
+  auto kern = simple ? li_topk_kernel<D_I, FP8, H_I, T, false> : li_topk_kernel<D_I, FP8, H_I, T, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
+  if (e != cudaSuccess) return cuda_fail(e, "li_topk: set shared memory size", err);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return cuda_fail(e, "li_topk: allow cluster > 8", err);
+
+  // Pick ring depth, cluster size and chunk with the occupancy API: how many clusters of each
+  // shape the GPU co-schedules decides the number of waves; within a wave the time is set by the
+  // HBM share of the resident CTAs, by how many bytes one SM keeps in flight, and by the
+  // select phase (which scans each CTA's chunk and does not overlap the stream).
+  struct Choice { int ns, c, chunk, smem; };
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, int>, Choice> memo;
+  const int forced_c = std::getenv("DSA_LI_CLUSTER") ? std::atoi(std::getenv("DSA_LI_CLUSTER")) : 0;
+  const int forced_ns = std::getenv("DSA_LI_STAGES") ? std::atoi(std::getenv("DSA_LI_STAGES")) : 0;
+  const auto key = std::make_tuple(dev.device, maxL, a.B * groups, forced_c, forced_ns);
+  Choice best{0, 0, 0, 0};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find(key);
+    if (it != memo.end()) best = it->second;
+  }
+  if (!best.c) {
+    double best_est = 1e300;
+    const long long clusters = (long long)a.B * groups;
+    for (int ns = 4; ns >= 2; --ns) {
+      if (forced_ns && ns != forced_ns) continue;
+      for (int c = 1; c <= kMaxCluster; ++c) {
+        if (forced_c && c != forced_c) continue;
+        const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
+        if (chunk > 65535 || (long long)chunk * c < maxL) continue;
+        const Layout lay(ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
+        const int smem = lay.total + 1024;
+        if (smem > dev.smem_optin) continue;
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3((unsigned)(c * clusters));
+        q.blockDim = dim3(kThreads);
+        q.dynamicSmemBytes = (size_t)smem;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)c;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        q.attrs = at;
+        q.numAttrs = 1;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &q) != cudaSuccess || active <= 0) {
+          cudaGetLastError();
+          continue;
+        }
+        const long long waves = (clusters + active - 1) / active;
+        const long long resident = std::min<long long>(clusters, active) * c;
+        const double per_sm = std::ceil((double)resident / dev.sm_count);
+        const double bytes_cta = (double)chunk * CF::kRowBytes;
+        const double hbm = 6.4e12, latency = 1.3e-6, sm_cap = 160e9;
+        const double sm_bw = std::min(sm_cap, per_sm * ns * CF::kTileBytes / latency);
+        const double t_stream = std::max(resident * bytes_cta / hbm, per_sm * bytes_cta / sm_bw);
+        const double t_select = 4e-6 + (double)chunk * T * 1.5e-9;
+        const double est = (double)waves * (t_stream + t_select);
+        if (est < best_est * 0.995) {
+          best_est = est;
+          best = Choice{ns, c, chunk, smem};
+        }
       }
     }
-  }
-  if (!best_c) {
-    err = "li_topk: no (ring depth, cluster size) fits shared memory for max_seq_len " +
-          std::to_string(a.max_seq_len);
-    return DSA_ERR_UNSUPPORTED;
-  }
-  if (const char* e = std::getenv("DSA_LI_CLUSTER")) {  // tuning override
-    const int c = std::atoi(e);
-    if (c >= 1 && c <= kMaxCluster) {
-      const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
-      const Layout lay(best_ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
-      if (lay.total + 1024 <= dev.smem_optin && chunk <= 65535) {
-        best_c = c;
-        best_chunk = chunk;
-        best_smem = lay.total + 1024;
-      }
+    if (!best.c) {
+      err = "li_topk: no (ring depth, cluster size) fits for max_seq_len " + std::to_string(a.max_seq_len);
+      return DSA_ERR_UNSUPPORTED;
     }
+    std::lock_guard<std::mutex> lock(mu);
+    memo[key] = best;
   }
+  const int best_ns = best.ns, best_c = best.c, best_chunk = best.chunk, best_smem = best.smem;
 
   CUtensorMap tm_k, tm_q;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -640,14 +676,6 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.q = a.q;
   p.k_pool = a.k_pool;
 
-  const bool simple = use_cuda_core_scores();
-  auto kern = simple ? li_topk_kernel<D_I, FP8, H_I, T, false> : li_topk_kernel<D_I, FP8, H_I, T, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, best_smem);
-  if (e != cudaSuccess) return cuda_fail(e, "li_topk: set shared memory size", err);
-  if (best_c > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return cuda_fail(e, "li_topk: allow cluster > 8", err);
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(best_c * a.B * groups));
   cfg.blockDim = dim3(kThreads);
@@ -670,8 +698,18 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
 
 }  // namespace li
 
+static dsa_status launch_li_topk_T(const dsa_li_args& a, int T, cudaStream_t stream, std::string& err);
+
 dsa_status launch_li_topk(const dsa_li_args& a, cudaStream_t stream, std::string& err) {
-  const int T = a.max_q_per_seq <= 1 ? 1 : (a.max_q_per_seq <= 2 ? 2 : 4);
+  // Tokens per cluster: all new tokens of a sequence up to 4 (4 x 64 heads = the widest MMA N);
+  // if a group of 4 does not fit shared memory at this context length, groups of 2.
+  int T = a.max_q_per_seq <= 1 ? 1 : (a.max_q_per_seq <= 2 ? 2 : 4);
+  dsa_status s = launch_li_topk_T(a, T, stream, err);
+  if (s == DSA_ERR_UNSUPPORTED && T == 4) s = launch_li_topk_T(a, 2, stream, err);
+  return s;
+}
+
+static dsa_status launch_li_topk_T(const dsa_li_args& a, int T, cudaStream_t stream, std::string& err) {
   const bool fp8 = a.dtype == DSA_FP8_E4M3;
   if (a.H_I == 64 && a.d_I == 128) {
     if (fp8) {

@@ -17,6 +17,7 @@
 namespace dsa {
 
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+constexpr uint32_t kSuspendHintNs = 20000u;                       // sleep per try_wait
 
 enum : int { kStatusOk = 0, kStatusDeviceCheck = 4, kStatusTimeout = 5 };
 
@@ -64,10 +65,24 @@ DSA_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// One potentially-blocking test of phase `parity`: the thread is suspended (issuing nothing)
+// until the phase completes or the hinted time (ns) passes.
 DSA_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of phase `parity`.
+DSA_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -82,7 +97,7 @@ DSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int*
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
@@ -117,6 +132,11 @@ DSA_DEV void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, 
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2),
       "r"(y3)
       : "memory");
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32); blocks in hardware.
+DSA_DEV void named_barrier(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 DSA_DEV void fence_proxy_async_smem() {

@@ -11,16 +11,19 @@
 // blocks); "Day0 Inference Adaptation ... CANN", section 3.1 (SFA reads the main attention KV at
 // the indexer's positions).
 //
-// Work decomposition.  A CTA serves one (query token, value half r, row split s):
-//   - Q[t] (128 heads x 576, bf16) is staged once by TMA into a 128-byte-swizzled K-major tile;
+// Work decomposition.  A CTA (16 warps) serves one (query token, value half r, row split s):
+//   - Q[t] (128 heads x 576, bf16) is split: dims 0..319 are written into TMEM (they are the A
+//     operand of the first 20 k-steps of Q.K^T), dims 320..575 are staged by TMA into a
+//     128-byte-swizzled K-major shared-memory tile;
 //   - the split's selected positions are translated to physical rows (page table) in shared
-//     memory, then each 32-row tile is gathered by TMA tile::gather4 (4 rows x 128 bytes per
-//     instruction) into a 2-stage ring: the same swizzled tile serves as the K-major B operand of
-//     Q.K^T (N = 32 rows, K = 576) and as the MN-major B operand of P.V (K = 32 rows, N = 256);
-//   - S = Q.K^T goes to a double-buffered TMEM accumulator; one thread per head (TMEM lane) masks,
-//     scales and exponentiates its row, writes P (bf16) back to TMEM and accumulates the row sum;
-//     the reference maximum only moves when a tile's maximum exceeds it by more than 2^8, and only
-//     then is the head's O row rescaled in TMEM;
+//     memory; eight gather warps then copy each 64-row tile with 16-byte cp.async (one row is 72
+//     chunks; empty slots are zero-filled) into a 2-stage ring laid out [box][row][128 B] with the
+//     128-byte swizzle, so the same tile is the K-major B operand of Q.K^T (N = 64 rows,
+//     K = 576) and the MN-major B operand of P.V (K = 64 rows, N = 256);
+//   - S = Q.K^T goes to TMEM; one thread per head (TMEM lane) masks, scales and exponentiates its
+//     row, writes P (bf16) back to TMEM and accumulates the row sum in fp32; the reference
+//     maximum only moves when a tile's maximum exceeds it by more than 2^8, and only then is the
+//     head's O row rescaled in TMEM;
 //   - O (128 x 256 fp32 = half of TMEM) accumulates P.V_r across tiles.
 // Each head's 128x512 fp32 O would fill all of TMEM, so the value columns are split over two
 // CTAs (r = 0, 1) that recompute the same S.  With several row splits the partial (o, lse) are
@@ -36,23 +39,35 @@
 namespace dsa {
 namespace sfa {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;      // 16 warps: 0-7 gather, 8 MMA, 12-15 softmax
+constexpr int kGatherThreads = 256;
+constexpr int kMmaWarp = 8;
+constexpr int kSoftmaxWarp0 = 12;
 constexpr int kHeads = 128;        // MMA M (heads are padded to 128)
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kDvHalf = 256;
-constexpr int kNT = 32;            // gathered rows per tile
+constexpr int kNT = 64;            // gathered rows per tile (MMA N of Q.K^T)
 constexpr int kStages = 2;
 constexpr int kBoxes = kDqk / 64;  // 9 column boxes of 64 bf16 (128 B)
-constexpr int kQBytes = kHeads * kDqk * 2;       // 147456
-constexpr int kTileBytes = kNT * kDqk * 2;       // 36864
+constexpr int kBoxBytes = kNT * 128;                        // one box of a tile: 8 KiB
+constexpr int kChunks = kNT * kDqk * 2 / 16;                // 16-byte chunks per tile (4608)
+// Q[t] is split: dims [0, kQTmemDims) live in TMEM (A operand of the first k-steps), the rest in
+// shared memory, so that two 72 KiB gather stages fit beside it.
+constexpr int kQTmemDims = 320;
+constexpr int kQSmemBox0 = kQTmemDims / 64;                 // first shared-memory box (5)
+constexpr int kQSmemBoxes = kBoxes - kQSmemBox0;            // 4
+constexpr int kQBytes = kHeads * kQSmemBoxes * 128;         // 65536
+constexpr int kTileBytes = kNT * kDqk * 2;                  // 73728
 constexpr int kMaxRows = 2048;     // row slots per CTA
 constexpr float kRescaleLog2 = 8.0f;
-// TMEM columns
-constexpr uint32_t kColS = 0;      // two 32-column S buffers
-constexpr uint32_t kColP = 64;     // P: 32 bf16 per lane = 16 columns
+// TMEM columns (512 in total)
+constexpr uint32_t kColS = 0;      // S: 64 columns
+constexpr uint32_t kColP = 64;     // P: 64 bf16 per lane = 32 columns
+constexpr uint32_t kColQ = 96;     // Q dims [0, 320): 160 columns (96..255)
 constexpr uint32_t kColO = 256;    // O half: 256 columns
 constexpr uint32_t kTmemCols = 512;
+static_assert(kChunks % kGatherThreads == 0, "gather split");
 
 struct Params {
   int B, n_q, H, K, max_pages, num_pages;
@@ -69,7 +84,7 @@ struct Params {
   float* ws_o;     // [n_q][2][splits][128][256] normalised partial outputs
   float* ws_lse;   // [n_q][2][splits][128] partial log2-sum-exp
   int* ws_count;   // [n_q][2] arrival counters (zero between calls)
-  const __nv_bfloat16* q;   // raw pointers for the CUDA-core variant
+  const __nv_bfloat16* q;
   const __nv_bfloat16* kv;
 };
 
@@ -77,20 +92,20 @@ struct Layout {
   static constexpr int q = 0;
   static constexpr int stages = q + kQBytes;
   static constexpr int rows = stages + kStages * kTileBytes;
-  static constexpr int ctl = rows + kMaxRows * 4;
+  static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
+  static constexpr int ctl = masks + kMaxRows / 8;
   static constexpr int total = ctl + 512;
 };
 
 struct Ctl {
-  uint64_t qbar;
+  uint64_t qbar, q_tmem;
   uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, pv_done, drain;
+  uint64_t s_full, s_free, p_full, pv_done, drain;
   uint32_t tmem_base;
   int abort;
-  int ntile;
   int last;  // this CTA merges the splits
   int nvalid;
+  int gather_go[3];  // poller's verdict per step (read by all gather threads after bar.sync)
 };
 
 DSA_DEV int find_seq(const int* q_start, int B, int t) {
@@ -107,15 +122,34 @@ DSA_DEV uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^x with the hardware approximation (flush-to-zero; 2^-inf = 0).  The weights are rounded to
+// bf16 right after, so its ~2-ulp fp32 error is far below what the output keeps.
+DSA_DEV float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+DSA_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed.
+DSA_DEV void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-               const Params p) {
+    sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* q_s = smem + Layout::q;
   uint8_t* st_s = smem + Layout::stages;
   int* rows_s = reinterpret_cast<int*>(smem + Layout::rows);
+  uint32_t* masks_s = reinterpret_cast<uint32_t*>(smem + Layout::masks);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + Layout::ctl);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -130,14 +164,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&ctl->qbar, 1);
+    mbar_init(&ctl->q_tmem, 128);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->full[s], kGatherThreads);
       mbar_init(&ctl->empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&ctl->s_full[a], 1);
-      mbar_init(&ctl->s_free[a], 128);
-    }
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->s_free, 128);
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->drain, 1);
@@ -145,30 +178,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->nvalid = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  // logical position -> physical row of every slot of this split (-1: empty or invalid)
+  // logical position -> physical row of every slot of this split (-1: empty or invalid), and a
+  // validity bit per slot (the softmax masks whole tiles from two words, with no per-slot loads)
   int last_valid = -1;
-  for (int i = tid; i < nslot; i += kThreads) {
-    const int j = p.idx[(size_t)t * p.K + slot0 + i];
+  for (int i0 = 0; i0 < kMaxRows; i0 += kThreads) {
+    const int i = i0 + tid;
     int row = -1;
-    if (j >= 0) {
-      if (j < L) {
-        const int pg = p.page_table[(size_t)b * p.max_pages + (j >> 6)];
-        if (pg >= 0 && pg < p.num_pages)
-          row = pg * 64 + (j & 63);
-        else
+    if (i < nslot) {
+      const int j = p.idx[(size_t)t * p.K + slot0 + i];
+      if (j >= 0) {
+        if (j < L) {
+          const int pg = p.page_table[(size_t)b * p.max_pages + (j >> 6)];
+          if (pg >= 0 && pg < p.num_pages)
+            row = pg * 64 + (j & 63);
+          else
+            report(p.status, kStatusDeviceCheck);
+        } else {
           report(p.status, kStatusDeviceCheck);
-      } else {
+        }
+      } else if (j < -1) {
         report(p.status, kStatusDeviceCheck);
       }
-    } else if (j < -1) {
-      report(p.status, kStatusDeviceCheck);
+      rows_s[i] = row;
+      if (row >= 0) last_valid = i;
     }
-    rows_s[i] = row;
-    if (row >= 0) last_valid = i;
+    const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
+    if (lane == 0) masks_s[i >> 5] = m;
   }
   // tiles needed: up to the last valid slot
   last_valid = __reduce_max_sync(0xffffffffu, last_valid + 1) - 1;
@@ -180,105 +219,172 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
 
-  float m_ref = -INFINITY, l_sum = 0.f;  // per-head state (threads 128..255)
+  // per-head state (softmax warps): reference maximum, the sum of the bf16 weights P.V uses
+  // (normalisation), and the fp32 sum of the unrounded weights (log-sum-exp)
+  float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- producer: Q once, then gathered tiles
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_kv);
-    if (ntile > 0) {
-      mbar_arrive_expect_tx(&ctl->qbar, kQBytes);
-      for (int bx = 0; bx < kBoxes; ++bx)
-        tma_load_2d(q_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, bx * 64, t * p.H);
+  if (warp < kGatherThreads / 32) {
+    // ---------------- gather: 16-byte cp.async of the selected latent rows into the ring,
+    // 128-byte swizzled [box][row][128 B] so the tile is a valid tcgen05 operand
+    const int g = tid;
+    const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.kv);
+    // One thread polls each barrier; the other gather warps sleep on a hardware barrier and
+    // then read the poller's verdict (a slot that is not rewritten before every gather thread
+    // has passed the next bar.sync, so all of them leave the loop at the same step).
+    if (ntile > 0) {  // Q dims 0..319 are staged in the ring until they are copied into TMEM
+      if (g == 0) ctl->gather_go[2] = mbar_wait(&ctl->q_tmem, 0, abort, p.status) ? 1 : 0;
+      named_barrier(1, kGatherThreads);
     }
-    for (int i = 0; i < ntile; ++i) {
+    const bool go = ntile == 0 || *reinterpret_cast<volatile int*>(&ctl->gather_go[2]) != 0;
+    for (int i = 0; go && i < ntile; ++i) {
       const int s = i % kStages;
-      if (i >= kStages &&
-          !mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status))
-        break;
-      mbar_arrive_expect_tx(&ctl->full[s], kTileBytes);
-      uint8_t* dst = st_s + s * kTileBytes;
-      for (int g = 0; g < kNT / 4; ++g) {
-        int r[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int slot = i * kNT + 4 * g + k;
-          const int row = slot < nslot ? rows_s[slot] : -1;
-          r[k] = row >= 0 ? row : 0;  // empty slots read row 0; their weight is exactly 0
-        }
-#pragma unroll
-        for (int bx = 0; bx < kBoxes; ++bx)
-          tma_gather4(dst + bx * (kNT * 128) + g * 512, &tm_kv, &ctl->full[s], bx * 64, r[0], r[1],
-                      r[2], r[3]);
+      if (i >= kStages) {
+        if (g == 0)
+          ctl->gather_go[i & 1] =
+              mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status) ? 1 : 0;
+        named_barrier(1, kGatherThreads);
+        if (*reinterpret_cast<volatile int*>(&ctl->gather_go[i & 1]) == 0) break;
       }
+      const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
+#pragma unroll 6
+      for (int k = 0; k < kChunks / kGatherThreads; ++k) {
+        const int c = g + k * kGatherThreads;
+        const int r = c / 72, ch = c % 72;
+        const int slot = i * kNT + r;
+        const int row = slot < nslot ? rows_s[slot] : -1;
+        const uint32_t dst = base + (uint32_t)((ch >> 3) * kBoxBytes + r * 128 +
+                                               (((ch & 7) ^ (r & 7)) << 4));
+        const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + ch * 16 : kv;
+        cp_async16(dst, src, row >= 0 ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(&ctl->full[s]);
     }
-    for (int i = max(0, ntile - kStages); i < ntile; ++i)
-      mbar_wait(&ctl->full[i % kStages], (uint32_t)(i / kStages) & 1u, abort, p.status);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ---------------- MMA issuer (and the shared-memory part of Q)
+    prefetch_tmap(&tm_q);
+    if (ntile > 0) {
+      // Q boxes 5..8 stay in q_s (A operand); boxes 0..4 land in the (still empty) gather ring
+      // and are moved into TMEM by the softmax warps
+      mbar_arrive_expect_tx(&ctl->qbar, kQBytes + kQSmemBox0 * kHeads * 128);
+      for (int bx = 0; bx < kQSmemBoxes; ++bx)
+        tma_load_2d(q_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, (kQSmemBox0 + bx) * 64, t * p.H);
+      for (int bx = 0; bx < kQSmemBox0; ++bx)
+        tma_load_2d(st_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, bx * 64, t * p.H);
+    }
     constexpr uint32_t idesc_qk = idesc_bf16(128, kNT);
     constexpr uint32_t idesc_pv = idesc_bf16(128, kDvHalf, /*b_mn_major=*/true);
-    const uint32_t q_addr = smem_u32(q_s), st_addr = smem_u32(st_s);
-    bool ok = ntile == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);
-    for (int i = 0; ok && i <= ntile; ++i) {
-      if (i < ntile) {
-        const int s = i % kStages, a = i & 1;
-        if (!mbar_wait(&ctl->full[s], (uint32_t)(i / kStages) & 1u, abort, p.status)) break;
-        if (i >= 2 && !mbar_wait(&ctl->s_free[a], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort, p.status))
-          break;
+    // Descriptors are built once; a k-step only moves the start address (the 14-bit address
+    // field cannot carry: every operand lies below 256 KiB).
+    const uint64_t qa_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
+    const uint64_t st_desc = sdesc_sw128(smem_u32(st_s), 16, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(st_s) + (uint32_t)(half * 4 * kBoxBytes), kBoxBytes, 1024);
+    bool ok = ntile == 0 || (mbar_wait(&ctl->qbar, 0, abort, p.status) &&
+                             mbar_wait(&ctl->q_tmem, 0, abort, p.status));
+    // Issue whichever is ready first: Q.K^T of the next tile (needs its rows and a free S) or
+    // P.V of the oldest tile whose weights are written (needs P).  Blocking on one of them while
+    // the other is ready would serialise gather, softmax and tensor work.
+    int nqk = 0, npv = 0;
+    uint64_t t_idle = 0;
+    while (ok && npv < ntile) {
+      bool progressed = false;
+      if (nqk < ntile && mbar_test(&ctl->full[nqk % kStages], (uint32_t)(nqk / kStages) & 1u) &&
+          (nqk == 0 || mbar_test(&ctl->s_free, (uint32_t)(nqk - 1) & 1u))) {
+        // the tile was written by cp.async (generic proxy); tcgen05.mma reads it (async proxy)
+        fence_proxy_async_smem();
         tc_fence_after();
-        const uint32_t d = tmem + kColS + (uint32_t)(a * kNT);
-        const uint32_t sb = st_addr + (uint32_t)(s * kTileBytes);
+        const uint64_t sb = st_desc + (uint64_t)(((nqk % kStages) * kTileBytes) >> 4);
 #pragma unroll 4
-        for (int kk = 0; kk < kDqk / 16; ++kk) {
-          const uint32_t bx = (uint32_t)kk >> 2, off = ((uint32_t)kk & 3u) * 32u;
-          const uint64_t ad = sdesc_sw128(q_addr + bx * (kHeads * 128) + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sb + bx * (kNT * 128) + off, 16, 1024);
-          mma_f16_ss(d, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kQTmemDims / 16; ++kk) {  // A = Q dims from TMEM
+          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+          mma_f16_ts(tmem + kColS, tmem + kColQ + (uint32_t)kk * 8u, sb + (off >> 4), idesc_qk,
+                     kk > 0 ? 1u : 0u);
         }
-        mma_commit(&ctl->s_full[a]);
+#pragma unroll 4
+        for (int kk = kQTmemDims / 16; kk < kDqk / 16; ++kk) {  // A = Q dims from shared memory
+          const uint32_t offb = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+          const uint32_t offa = (uint32_t)((kk >> 2) - kQSmemBox0) * (kHeads * 128) + (uint32_t)(kk & 3) * 32u;
+          mma_f16_ss(tmem + kColS, qa_desc + (offa >> 4), sb + (offb >> 4), idesc_qk, 1u);
+        }
+        mma_commit(&ctl->s_full);
+        ++nqk;
+        progressed = true;
       }
-      if (i >= 1) {
-        const int ip = i - 1, s = ip % kStages;
-        if (!mbar_wait(&ctl->p_full, (uint32_t)ip & 1u, abort, p.status)) break;
+      if (npv < nqk && mbar_test(&ctl->p_full, (uint32_t)npv & 1u)) {
         tc_fence_after();
-        const uint32_t sb = st_addr + (uint32_t)(s * kTileBytes) + (uint32_t)(half * 4 * kNT * 128);
+        const int s = npv % kStages;
+        const uint64_t vb = v_desc + (uint64_t)((s * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kNT / 16; ++kk) {
           // B = V rows [16kk, 16kk+16) x this half's 256 value columns, MN-major:
-          // 64-column blocks kNT*128 bytes apart (lbo), 8-row groups 1024 bytes apart (sbo)
-          const uint64_t bd = sdesc_sw128(sb + (uint32_t)kk * 2048u, kNT * 128, 1024);
-          mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)kk * 8u, bd, idesc_pv,
-                     (ip > 0 || kk > 0) ? 1u : 0u);
+          // 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024 bytes apart (sbo)
+          mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)kk * 8u, vb + (uint64_t)(kk * 2048 >> 4),
+                     idesc_pv, (npv > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&ctl->pv_done);
         mma_commit(&ctl->empty[s]);
+        ++npv;
+        progressed = true;
+      }
+      if (progressed) {
+        t_idle = 0;
+      } else {
+        const uint64_t now = globaltimer();
+        if (t_idle == 0) t_idle = now;
+        if (*abort) break;
+        if (now - t_idle > kWaitLimitNs) {
+          *abort = 1;
+          report(p.status, kStatusTimeout);
+          break;
+        }
       }
     }
     mma_commit(&ctl->drain);
     mbar_wait(&ctl->drain, 0, abort, p.status);
-  } else if (warp >= 4) {
+  } else if (warp >= kSoftmaxWarp0) {
     // ---------------- softmax: one thread per head row (TMEM lane)
-    const int qd = warp - 4, h = qd * 32 + lane;
+    const int qd = warp - kSoftmaxWarp0, h = qd * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    if (ntile > 0) {
+      // Q[t][h][0:320] (staged by TMA, 128-byte swizzled) -> TMEM columns kColQ.. (two bf16 per
+      // 32-bit column); heads >= H are 0
+      const bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
+      (void)ok;
+#pragma unroll 1
+      for (int c = 0; c < kQSmemBox0; ++c) {
+        uint32_t r[32];
+        const uint8_t* box = st_s + c * (kHeads * 128) + h * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = h < p.H ? *reinterpret_cast<const uint4*>(box + ((v ^ (h & 7)) << 4))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+        }
+        tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32), r);
+        tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32 + 16), r + 16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctl->q_tmem);
+    }
     for (int i = 0; i < ntile; ++i) {
-      const int a = i & 1;
-      bool ok = mbar_wait(&ctl->s_full[a], (uint32_t)(i >> 1) & 1u, abort, p.status);
+      bool ok = mbar_wait(&ctl->s_full, (uint32_t)i & 1u, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      uint32_t sr[32];
-      tmem_ld_x32(lane_addr + kColS + (uint32_t)(a * kNT), sr);
+      uint32_t sr[64];
+      tmem_ld_x32(lane_addr + kColS, sr);
+      tmem_ld_x32(lane_addr + kColS + 32, sr + 32);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&ctl->s_free[a]);
-      float z[32];
+      mbar_arrive(&ctl->s_free);
       float mt = -INFINITY;
+      const uint32_t vm0 = masks_s[2 * i], vm1 = masks_s[2 * i + 1];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int slot = i * kNT + c;
-        const bool valid = slot < nslot && rows_s[slot] >= 0;
-        z[c] = valid ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, z[c]);
+      for (int c = 0; c < kNT; ++c) {
+        const bool valid = ((c < 32 ? vm0 : vm1) >> (c & 31)) & 1u;
+        const float z = valid ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
+        sr[c] = __float_as_uint(z);
+        mt = fmaxf(mt, z);
       }
       if (i >= 1) {
         ok = mbar_wait(&ctl->pv_done, (uint32_t)(i - 1) & 1u, abort, p.status);
@@ -300,21 +406,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_x16(lane_addr + kColO + (uint32_t)(c * 32 + 16), o + 16);
         }
         tmem_st_wait();
-        if (need) l_sum *= alpha;
+        if (need) {
+          l_sum *= alpha;
+          l_exact *= alpha;
+        }
       }
       if (need) m_ref = mt;
-      uint32_t pk[16];
-      float ls = 0.f;
+      uint32_t pk[32];
+      float ls = 0.f, le = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float p0 = m_ref == -INFINITY ? 0.f : exp2f(z[2 * c] - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : exp2f(z[2 * c + 1] - m_ref);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * c]) - m_ref);
+        const float p1 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * c + 1]) - m_ref);
         pk[c] = pack_bf16(p0, p1);
-        const __nv_bfloat162 r = *reinterpret_cast<__nv_bfloat162*>(&pk[c]);
-        ls += __bfloat162float(r.x) + __bfloat162float(r.y);  // sum what P.V actually uses
+        const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&pk[c]);
+        ls += __bfloat162float(r.x) + __bfloat162float(r.y);
+        le += p0 + p1;
       }
       l_sum += ls;
+      l_exact += le;
       tmem_st_x16(lane_addr + kColP, pk);
+      tmem_st_x16(lane_addr + kColP + 16, pk + 16);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->p_full);
@@ -326,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---------------- epilogue
     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    const float lse2 = l_sum > 0.f ? m_ref + log2f(l_sum) : -INFINITY;
+    const float lse2 = l_exact > 0.f ? m_ref + log2f(l_exact) : -INFINITY;
     if (p.splits == 1) {
       __nv_bfloat16* orow = p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf;
 #pragma unroll 1
@@ -378,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -395,21 +507,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ctl->last) return;
   __threadfence();
   const size_t unit0 = ((size_t)t * 2 + half) * p.splits;
-  // 256 threads: head h = tid / 2, value columns [128 * (tid & 1), +128)
-  const int h = tid >> 1, c0 = (tid & 1) * 128;
+  // 512 threads: head h = tid / 4, value columns [64 * (tid & 3), +64)
+  const int h = tid >> 2, c0 = (tid & 3) * 64;
   float M = -INFINITY;
   for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.ws_lse + (unit0 + s) * kHeads + h));
   float W = 0.f;
-  float acc[128];
+  float acc[64];
 #pragma unroll
-  for (int k = 0; k < 128; ++k) acc[k] = 0.f;
+  for (int k = 0; k < 64; ++k) acc[k] = 0.f;
   for (int s = 0; s < p.splits; ++s) {
     const float ls = __ldcg(p.ws_lse + (unit0 + s) * kHeads + h);
     const float wgt = (M == -INFINITY || ls == -INFINITY) ? 0.f : exp2f(ls - M);
     W += wgt;
     const float4* src = reinterpret_cast<const float4*>(p.ws_o + ((unit0 + s) * kHeads + h) * kDvHalf + c0);
 #pragma unroll
-    for (int v = 0; v < 32; ++v) {
+    for (int v = 0; v < 16; ++v) {
       const float4 x = __ldcg(src + v);
       acc[4 * v] = fmaf(wgt, x.x, acc[4 * v]);
       acc[4 * v + 1] = fmaf(wgt, x.y, acc[4 * v + 1]);
@@ -421,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float inv = W > 0.f ? 1.f / W : 0.f;
     uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf + c0);
 #pragma unroll
-    for (int v = 0; v < 16; ++v) {
+    for (int v = 0; v < 8; ++v) {
       uint4 w;
       w.x = pack_bf16(acc[8 * v] * inv, acc[8 * v + 1] * inv);
       w.y = pack_bf16(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv);
@@ -587,12 +699,9 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "sfa (cuda-core): launch", err);
   }
 
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q;
   if (!encode_tmap_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDqk, (uint64_t)a.n_q * a.H,
                       kDqk * 2, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_128B, err))
-    return DSA_ERR_CUDA;
-  if (!encode_tmap_2d(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.kv_pool, kDqk,
-                      (uint64_t)a.num_pages * 64, kDqk * 2, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, err))
     return DSA_ERR_CUDA;
   const int smem = Layout::total + 1024;
   cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -601,7 +710,7 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   if (std::getenv("DSA_VERBOSE"))
     std::fprintf(stderr, "[dsa] sfa %s splits=%d rows_per=%d grid=%u smem=%d\n",
                  prefill ? "prefill" : "decode", pl.splits, pl.rows_per, grid, smem);
-  sfa_kernel<<<grid, kThreads, smem, stream>>>(tm_q, tm_kv, p);
+  sfa_kernel<<<grid, kThreads, smem, stream>>>(tm_q, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sfa: launch", err);
   return DSA_OK;
