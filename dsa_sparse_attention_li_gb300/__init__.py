@@ -30,8 +30,12 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_C
 DSA_BF16, DSA_FP8_E4M3 = 0, 1
 
 SYMBOLS = ["dsa_status_string", "dsa_last_error", "dsa_abi_version", "dsa_li_topk",
-           "dsa_sfa_workspace_bytes", "dsa_sfa_decode", "dsa_sfa_prefill", "dsa_page_bytes",
-           "dsa_page_table_validate", "dsa_cache_write"]
+           "dsa_sfa_workspace_bytes", "dsa_sfa_decode", "dsa_sfa_prefill",
+           "dsa_sfa_decode_static", "dsa_page_bytes", "dsa_page_table_validate",
+           "dsa_cache_write"]
+
+# Capacity of the library's fixed scratch array used by dsa_sfa_decode_static.
+SFA_STATIC_SCRATCH_BYTES = 20 * 1024 * 1024
 
 
 class DsaError(RuntimeError):
@@ -77,7 +81,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.dsa_abi_version.restype = ctypes.c_int
     lib.dsa_li_topk.argtypes = [ctypes.POINTER(LiArgs), P]
     lib.dsa_li_topk.restype = ctypes.c_int
-    for f in (lib.dsa_sfa_decode, lib.dsa_sfa_prefill):
+    for f in (lib.dsa_sfa_decode, lib.dsa_sfa_prefill, lib.dsa_sfa_decode_static):
         f.argtypes = [ctypes.POINTER(SfaArgs), P]
         f.restype = ctypes.c_int
     lib.dsa_sfa_workspace_bytes.argtypes = [ctypes.POINTER(SfaArgs)]
@@ -219,6 +223,25 @@ def _sfa(entry, name, q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax
 def sfa_decode(q, kv_pool, page_table, seq_lens, q_start, idx, **kw):
     """Sparse attention for few tokens per sequence (row splits merged through a workspace)."""
     return _sfa("dsa_sfa_decode", "sfa_decode", q, kv_pool, page_table, seq_lens, q_start, idx, **kw)
+
+
+def sfa_decode_static(q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax_scale,
+                      max_seq_len=None, max_q_per_seq=None, out=None, lse=None, status=None,
+                      stream=None):
+    """sfa_decode for callers that cannot allocate: the split-merge scratch is the library's own
+    fixed device array (SFA_STATIC_SCRATCH_BYTES, shared by every call on the device, so calls
+    must not overlap on the GPU).  Only the outputs are allocated here, and only when not given."""
+    lib = load()
+    n_q, H, _ = q.shape
+    if out is None:
+        out = torch.empty((n_q, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((n_q, H), dtype=torch.float32, device=q.device)
+    a = sfa_args(q, kv_pool, page_table, seq_lens, q_start, idx, softmax_scale=softmax_scale,
+                 max_seq_len=max_seq_len, max_q_per_seq=max_q_per_seq, out=out, lse=lse,
+                 status=status, workspace=None)
+    _check(lib.dsa_sfa_decode_static(ctypes.byref(a), _stream(stream)), "dsa_sfa_decode_static")
+    return out, lse
 
 
 def sfa_prefill(q, kv_pool, page_table, seq_lens, q_start, idx, **kw):

@@ -25,6 +25,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 namespace dsa {
 
+void set_last_error(const std::string& why) { g_last_error = why; }
+
 bool device_info(DeviceInfo& info, std::string& err) {
   static std::mutex mu;
   static std::vector<DeviceInfo> cache(64);

@@ -25,6 +25,9 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle, std::string& err);
 
+// Sets the calling thread's dsa_last_error() text.
+void set_last_error(const std::string& why);
+
 // Device properties of the current device (cached per device).
 struct DeviceInfo {
   int device = -1;

@@ -156,6 +156,26 @@ size_t dsa_sfa_workspace_bytes(const dsa_sfa_args* args);
 dsa_status dsa_sfa_decode(const dsa_sfa_args* args, dsa_stream_t stream);
 dsa_status dsa_sfa_prefill(const dsa_sfa_args* args, dsa_stream_t stream);
 
+/*
+ * dsa_sfa_decode without a caller workspace, for callers that cannot allocate device memory: an
+ * operator inside a framework that plans all device memory itself and passes the operator only
+ * its inputs and outputs, or a path on which allocating is not allowed.  The pages have no
+ * counterpart of this; it is an interface convenience of this library.
+ *
+ * The split-merge scratch is a fixed device array of DSA_SFA_STATIC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads the library until the process exits.  args->workspace and
+ * args->workspace_bytes are ignored; everything else is exactly dsa_sfa_decode (same kernel, same
+ * result).  Arguments whose dsa_sfa_workspace_bytes() exceeds the capacity are rejected with
+ * DSA_ERR_UNSUPPORTED and a reason in dsa_last_error().  No call allocates or frees memory.
+ *  - The first call on a device looks up the array's device address (once per device, with that
+ *    device current); make that first call before capturing a stream.
+ *  - All calls on a device share the one array, which keeps the last call's contents; the call
+ *    clears what must start at zero.  Calls whose work overlaps on the GPU (other streams, other
+ *    host threads) race on the array: serialise them.
+ */
+#define DSA_SFA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
+dsa_status dsa_sfa_decode_static(const dsa_sfa_args* args, dsa_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------ */
 /* Cache layout and page-table helpers                                                         */
 /* ------------------------------------------------------------------------------------------ */
