@@ -135,6 +135,11 @@ DSA_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+// Asynchronous L2 prefetch of `bytes` (a multiple of 16) starting at a 16-byte aligned address.
+DSA_DEV void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 DSA_DEV void cp_async_arrive_noinc(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
@@ -182,6 +187,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  __syncthreads();  // barriers initialised
+  if (warp == kMmaWarp && lane == 0 && nslot > 0) {
+    // Q boxes 5..8 stay in q_s (A operand); boxes 0..4 land in the (still empty) gather ring and
+    // are moved into TMEM by the softmax warps.  Issued before the row translation below so the
+    // load overlaps it.
+    prefetch_tmap(&tm_q);
+    mbar_arrive_expect_tx(&ctl->qbar, kQBytes + kQSmemBox0 * kHeads * 128);
+    for (int bx = 0; bx < kQSmemBoxes; ++bx)
+      tma_load_2d(q_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, (kQSmemBox0 + bx) * 64, t * p.H);
+    for (int bx = 0; bx < kQSmemBox0; ++bx)
+      tma_load_2d(st_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, bx * 64, t * p.H);
+  }
   // logical position -> physical row of every slot of this split (-1: empty or invalid), and a
   // validity bit per slot (the softmax masks whole tiles from two words, with no per-slot loads)
   int last_valid = -1;
@@ -228,6 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128-byte swizzled [box][row][128 B] so the tile is a valid tcgen05 operand
     const int g = tid;
     const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.kv);
+    // Warm L2 with the rows of the first tiles while Q is staged.
+    for (int slot = g; slot < min(nslot, 2 * kStages * kNT); slot += kGatherThreads) {
+      const int row = rows_s[slot];
+      if (row >= 0) l2_prefetch_bulk(kv + (size_t)row * (kDqk * 2), kDqk * 2);
+    }
     // One thread polls each barrier; the other gather warps sleep on a hardware barrier and
     // then read the poller's verdict (a slot that is not rewritten before every gather thread
     // has passed the next bar.sync, so all of them leave the loop at the same step).
@@ -258,20 +280,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async16(dst, src, row >= 0 ? 16u : 0u);
       }
       cp_async_arrive_noinc(&ctl->full[s]);
+      // Warm L2 with the rows of the tile that will reuse this stage, so its copies return at L2
+      // latency once the stage frees (one bulk prefetch per 1152-byte row).
+      const int pf = i + 2 * kStages;
+      if (pf < ntile && g < kNT) {
+        const int slot = pf * kNT + g;
+        const int row = slot < nslot ? rows_s[slot] : -1;
+        if (row >= 0) l2_prefetch_bulk(kv + (size_t)row * (kDqk * 2), kDqk * 2);
+      }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp && lane == 0) {
-    // ---------------- MMA issuer (and the shared-memory part of Q)
-    prefetch_tmap(&tm_q);
-    if (ntile > 0) {
-      // Q boxes 5..8 stay in q_s (A operand); boxes 0..4 land in the (still empty) gather ring
-      // and are moved into TMEM by the softmax warps
-      mbar_arrive_expect_tx(&ctl->qbar, kQBytes + kQSmemBox0 * kHeads * 128);
-      for (int bx = 0; bx < kQSmemBoxes; ++bx)
-        tma_load_2d(q_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, (kQSmemBox0 + bx) * 64, t * p.H);
-      for (int bx = 0; bx < kQSmemBox0; ++bx)
-        tma_load_2d(st_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, bx * 64, t * p.H);
-    }
+    // ---------------- MMA issuer
     constexpr uint32_t idesc_qk = idesc_bf16(128, kNT);
     constexpr uint32_t idesc_pv = idesc_bf16(128, kDvHalf, /*b_mn_major=*/true);
     // Descriptors are built once; a k-step only moves the start address (the 14-bit address
@@ -279,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t qa_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
     const uint64_t st_desc = sdesc_sw128(smem_u32(st_s), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(st_s) + (uint32_t)(half * 4 * kBoxBytes), kBoxBytes, 1024);
-    bool ok = ntile == 0 || (mbar_wait(&ctl->qbar, 0, abort, p.status) &&
-                             mbar_wait(&ctl->q_tmem, 0, abort, p.status));
+    bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
+    ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
     // Issue whichever is ready first: Q.K^T of the next tile (needs its rows and a free S) or
     // P.V of the oldest tile whose weights are written (needs P).  Blocking on one of them while
     // the other is ready would serialise gather, softmax and tensor work.
@@ -507,42 +527,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!ctl->last) return;
   __threadfence();
   const size_t unit0 = ((size_t)t * 2 + half) * p.splits;
-  // 512 threads: head h = tid / 4, value columns [64 * (tid & 3), +64)
-  const int h = tid >> 2, c0 = (tid & 3) * 64;
-  float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.ws_lse + (unit0 + s) * kHeads + h));
-  float W = 0.f;
-  float acc[64];
-#pragma unroll
-  for (int k = 0; k < 64; ++k) acc[k] = 0.f;
-  for (int s = 0; s < p.splits; ++s) {
-    const float ls = __ldcg(p.ws_lse + (unit0 + s) * kHeads + h);
-    const float wgt = (M == -INFINITY || ls == -INFINITY) ? 0.f : exp2f(ls - M);
-    W += wgt;
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + ((unit0 + s) * kHeads + h) * kDvHalf + c0);
-#pragma unroll
-    for (int v = 0; v < 16; ++v) {
-      const float4 x = __ldcg(src + v);
-      acc[4 * v] = fmaf(wgt, x.x, acc[4 * v]);
-      acc[4 * v + 1] = fmaf(wgt, x.y, acc[4 * v + 1]);
-      acc[4 * v + 2] = fmaf(wgt, x.z, acc[4 * v + 2]);
-      acc[4 * v + 3] = fmaf(wgt, x.w, acc[4 * v + 3]);
+  // Coalesced merge: thread -> (4 value columns c4, heads h0 + 8k); a warp reads 512 contiguous
+  // bytes of one head row per load.
+  float* wgt = reinterpret_cast<float*>(st_s);  // [splits][128] merge weights (ring is free now)
+  float* winv = wgt + p.splits * kHeads;        // [128] 1 / sum of weights
+  if (tid < kHeads) {
+    const int h = tid;
+    float M = -INFINITY;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(p.ws_lse + (unit0 + s) * kHeads + h));
+    float W = 0.f;
+    for (int s = 0; s < p.splits; ++s) {
+      const float ls = __ldcg(p.ws_lse + (unit0 + s) * kHeads + h);
+      const float w = (M == -INFINITY || ls == -INFINITY) ? 0.f : exp2f(ls - M);
+      wgt[s * kHeads + h] = w;
+      W += w;
     }
-  }
-  if (h < p.H) {
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf + c0);
-#pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      uint4 w;
-      w.x = pack_bf16(acc[8 * v] * inv, acc[8 * v + 1] * inv);
-      w.y = pack_bf16(acc[8 * v + 2] * inv, acc[8 * v + 3] * inv);
-      w.z = pack_bf16(acc[8 * v + 4] * inv, acc[8 * v + 5] * inv);
-      w.w = pack_bf16(acc[8 * v + 6] * inv, acc[8 * v + 7] * inv);
-      dst[v] = w;
-    }
-    if (half == 0 && c0 == 0 && p.lse)
+    winv[h] = W > 0.f ? 1.f / W : 0.f;
+    if (half == 0 && h < p.H && p.lse)
       p.lse[(size_t)t * p.H + h] = W > 0.f ? (M + log2f(W)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  const int c4 = (tid & 63) * 4, h0 = tid >> 6;
+  constexpr int kHeadStep = kThreads / 64;      // 8 head groups
+  constexpr int kBatch = 8;                     // heads per thread with loads in flight together
+#pragma unroll 1
+  for (int hb = h0; hb < kHeads; hb += kHeadStep * kBatch) {
+    float4 acc[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.splits; ++s) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        x[k] = __ldcg(reinterpret_cast<const float4*>(
+            p.ws_o + ((unit0 + s) * kHeads + hb + k * kHeadStep) * kDvHalf + c4));
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float w = wgt[s * kHeads + hb + k * kHeadStep];
+        acc[k].x = fmaf(w, x[k].x, acc[k].x);
+        acc[k].y = fmaf(w, x[k].y, acc[k].y);
+        acc[k].z = fmaf(w, x[k].z, acc[k].z);
+        acc[k].w = fmaf(w, x[k].w, acc[k].w);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int h = hb + k * kHeadStep;
+      if (h < p.H) {
+        const float inv = winv[h];
+        uint2 v;
+        v.x = pack_bf16(acc[k].x * inv, acc[k].y * inv);
+        v.y = pack_bf16(acc[k].z * inv, acc[k].w * inv);
+        *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf + c4) = v;
+      }
+    }
   }
 }
 
