@@ -38,7 +38,8 @@
 namespace dsa {
 namespace li {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;       // 12 warps: 0 TMA, 1 MMA, 4-7 and 8-11 two epilogue groups
+constexpr int kHistThreads = 256;   // threads that own 8 histogram bins each in the select
 constexpr int kTileKeys = 128;
 constexpr int kHistWords = 1024;  // 2048 radix bins, two 16-bit counters per 32-bit word
 constexpr int kMaxCluster = 16;
@@ -104,7 +105,7 @@ struct Ctl {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  uint32_t scan[8];
+  uint32_t scan[kThreads / 32];
   int need[4];        // remaining count to select among the current prefix
   uint32_t prefix[4]; // key prefix fixed so far
   int radix[4];       // token needs a radix select (visible > K)
@@ -112,7 +113,7 @@ struct Ctl {
   int cnt_gt[4], cnt_eq[4];  // this CTA's counts (read by the cluster)
   int offset[4], quota[4];
   int found_bin[4], found_need[4];
-  int wgt[4][8], weq[4][8];  // per-warp counts above / at the threshold
+  int wgt[4][kThreads / 32], weq[4][kThreads / 32];  // per-warp counts above / at the threshold
 };
 
 // ---- block-level scans over 256 threads ----
@@ -296,10 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&ctl->drain);
       mbar_wait(&ctl->drain, 0, abort, p.status);
     } else if (warp >= 4) {
-      const int qd = warp - 4;  // TMEM lane quadrant of this warp
+      // Two epilogue groups: warps 4-7 take accumulator 0 (even tiles), warps 8-11 accumulator 1
+      // (odd tiles), so two tiles are reduced at once.
+      const int grp = (warp - 4) >> 2;
+      const int qd = warp & 3;  // TMEM lane quadrant of this warp
       const int row = qd * 32 + lane;
-      for (int i = 0; i < ntile; ++i) {
-        const int a = i & 1;
+      for (int i = grp; i < ntile; i += 2) {
+        const int a = grp;
         const int j = lo + i * kTileKeys + row;
         float ks = 1.f;
         if (FP8) {
@@ -310,26 +314,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.ld below needs the whole warp
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(a * CF::kNCol);
-#pragma unroll
+#pragma unroll 1
         for (int tt = 0; tt < T; ++tt) {
-          float s = 0.f;
+          float s;
           if constexpr (H_I == 64) {
-            uint32_t r[32];
+            uint32_t r[64];
+            tmem_ld_x32(taddr + (uint32_t)(tt * H_I), r);
+            tmem_ld_x32(taddr + (uint32_t)(tt * H_I + 32), r + 32);
+            tmem_ld_wait();
+            // four independent partial sums (the weights are read as float4 broadcasts)
+            const float4* w4 = reinterpret_cast<const float4*>(wts + tt * H_I);
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              tmem_ld_x32(taddr + (uint32_t)(tt * H_I + half * 32), r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int h = 0; h < 32; ++h)
-                s = fmaf(wts[tt * H_I + half * 32 + h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+            for (int q = 0; q < 16; ++q) {
+              const float4 w = w4[q];
+              a0 = fmaf(w.x, fmaxf(__uint_as_float(r[4 * q + 0]), 0.f), a0);
+              a1 = fmaf(w.y, fmaxf(__uint_as_float(r[4 * q + 1]), 0.f), a1);
+              a2 = fmaf(w.z, fmaxf(__uint_as_float(r[4 * q + 2]), 0.f), a2);
+              a3 = fmaf(w.w, fmaxf(__uint_as_float(r[4 * q + 3]), 0.f), a3);
             }
+            s = (a0 + a1) + (a2 + a3);
           } else {
             uint32_t r[8];
             tmem_ld_x8(taddr + (uint32_t)(tt * H_I), r);
             tmem_ld_wait();
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int h = 0; h < 8; ++h)
-              s = fmaf(wts[tt * H_I + h], fmaxf(__uint_as_float(r[h]), 0.f), s);
+            for (int h = 0; h < 8; h += 2) {
+              a0 = fmaf(wts[tt * H_I + h], fmaxf(__uint_as_float(r[h]), 0.f), a0);
+              a1 = fmaf(wts[tt * H_I + h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.f), a1);
+            }
+            s = a0 + a1;
           }
           if (FP8) s *= ks;
           const bool valid = tt < nt && j < lo + p.chunk && j <= pos0 + tt;
@@ -427,13 +442,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tt = 0; tt < T; ++tt) {
         if (!ctl->radix[tt]) continue;  // uniform over the block
         uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        const uint32_t* h = hb + tt * kHistWords + 4 * tid;
-        for (int r = 0; r < p.C; ++r) {
-          const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
-          cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
-          cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
-          cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
-          cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
+        if (tid < kHistThreads) {
+          const uint32_t* h = hb + tt * kHistWords + 4 * tid;
+          for (int r = 0; r < p.C; ++r) {
+            const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
+            cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
+            cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
+            cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
+            cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
+          }
         }
         uint32_t sum = 0;
 #pragma unroll
@@ -596,7 +613,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   if (!best.c) {
     double best_est = 1e300;
     const long long clusters = (long long)a.B * groups;
-    for (int ns = 4; ns >= 2; --ns) {
+    for (int ns = 8; ns >= 2; --ns) {
       if (forced_ns && ns != forced_ns) continue;
       for (int c = 1; c <= kMaxCluster; ++c) {
         if (forced_c && c != forced_c) continue;
