@@ -43,6 +43,7 @@ constexpr int kHistThreads = 256;   // threads that own 8 histogram bins each in
 constexpr int kTileKeys = 128;
 constexpr int kHistWords = 1024;  // 2048 radix bins, two 16-bit counters per 32-bit word
 constexpr int kMaxCluster = 16;
+constexpr int kCtlBytes = 2560;   // shared control block (mbarriers, counters), sizeof(Ctl) rounded up
 
 struct Params {
   int B, n_q, K, max_pages, num_pages;
@@ -92,7 +93,7 @@ struct Layout {
     hist = scores + T * chunk * 4;
     pages = hist + 2 * T * kHistWords * 4;
     ctl = pages + ((2 * (chunk / kTileKeys) * 4 + 127) / 128) * 128;
-    total = ctl + 1024;
+    total = ctl + kCtlBytes;
   }
 };
 
@@ -114,7 +115,14 @@ struct Ctl {
   int offset[4], quota[4];
   int found_bin[4], found_need[4];
   int wgt[4][kThreads / 32], weq[4][kThreads / 32];  // per-warp counts above / at the threshold
+  // candidate path of the select (see the select phase)
+  int cand_total[4];          // keys of the whole cluster in the threshold bin of the first pass
+  int own_cnt[4];             // this CTA's candidates (read by the cluster)
+  int rn[4][kMaxCluster], roff[4][kMaxCluster];    // candidates per rank and their offsets
+  int rsure[4][kMaxCluster];  // per rank: keys certainly selected (above the first-pass bin)
+  int rgt[4][kMaxCluster], req[4][kMaxCluster];    // per rank: candidates above / at the threshold
 };
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 // ---- block-level scans over 256 threads ----
 
@@ -135,6 +143,58 @@ DSA_DEV uint32_t block_excl_suffix(uint32_t v, uint32_t* scratch) {
     if (w > warp) above += scratch[w];
   __syncthreads();
   return above + x - v;
+}
+
+// Inclusive sum over the lanes of the warp.
+DSA_DEV uint32_t warp_incl_scan(uint32_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// Set bits of each 4-bit group g < 4 of x, counted into byte g.  Sums of such words over a warp
+// stay below 256 per byte, so one scan of the packed word gives four prefix counts at once.
+DSA_DEV uint32_t nibble_counts(uint32_t x) {
+  uint32_t y = (x & 0xfu) | ((x & 0xf0u) << 4) | ((x & 0xf00u) << 8) | ((x & 0xf000u) << 12);
+  y = (y & 0x05050505u) + ((y >> 1) & 0x05050505u);
+  return (y & 0x03030303u) + ((y >> 2) & 0x03030303u);
+}
+
+// In a 2048-bin histogram (packed 16-bit counters, 1024 words) of this CTA, finds the bin that
+// holds the need-th largest key counting from the top bin: ctl->found_bin / found_need.
+template <typename CtlT>
+DSA_DEV void find_bin_local(const uint32_t* h, uint32_t need, int tt, CtlT* ctl) {
+  const int tid = threadIdx.x;
+  uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (tid < 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(h + 4 * tid);
+    cnt[0] = v.x & 0xffffu; cnt[1] = v.x >> 16;
+    cnt[2] = v.y & 0xffffu; cnt[3] = v.y >> 16;
+    cnt[4] = v.z & 0xffffu; cnt[5] = v.z >> 16;
+    cnt[6] = v.w & 0xffffu; cnt[7] = v.w >> 16;
+  }
+  uint32_t sum = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sum += cnt[k];
+  if (tid == 0) {
+    ctl->found_bin[tt] = 0;
+    ctl->found_need[tt] = 1;
+  }
+  const uint32_t above = block_excl_suffix(sum, ctl->scan);
+  uint32_t run = above;
+#pragma unroll
+  for (int k = 7; k >= 0; --k) {
+    if (run < need && run + cnt[k] >= need) {
+      ctl->found_bin[tt] = 8 * tid + k;
+      ctl->found_need[tt] = (int)(need - run);
+    }
+    run += cnt[k];
+  }
+  __syncthreads();
 }
 
 DSA_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -246,6 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int bx = 0; bx < CF::kBoxes; ++bx)
         tma_load_2d(q_s + bx * CF::kNCol * 128, &tm_q, &ctl->qbar, bx * (128 / CF::kElt),
                     t0 * H_I);
+      // With one token group per sequence every key row is read by exactly one CTA: stream it
+      // with the evict-first L2 policy.  Otherwise other groups re-read it from L2.
+      const bool read_once = p.groups == 1;
+      const uint64_t pol = l2_policy_evict_first();
       for (int i = 0; i < ntile; ++i) {
         const int s = i % p.nstage;
         const uint32_t ph = (uint32_t)(i / p.nstage) & 1u;
@@ -256,8 +320,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* st = stage_base + (size_t)s * CF::kTileBytes;
         for (int bx = 0; bx < CF::kBoxes; ++bx) {
           const int x = bx * (128 / CF::kElt);
-          if (pg0 >= 0) tma_load_2d(st + bx * 16384, &tm_k, &ctl->full[s], x, pg0 * 64);
-          if (pg1 >= 0) tma_load_2d(st + bx * 16384 + 8192, &tm_k, &ctl->full[s], x, pg1 * 64);
+          if (read_once) {
+            if (pg0 >= 0) tma_load_2d_hint(st + bx * 16384, &tm_k, &ctl->full[s], x, pg0 * 64, pol);
+            if (pg1 >= 0)
+              tma_load_2d_hint(st + bx * 16384 + 8192, &tm_k, &ctl->full[s], x, pg1 * 64, pol);
+          } else {
+            if (pg0 >= 0) tma_load_2d(st + bx * 16384, &tm_k, &ctl->full[s], x, pg0 * 64);
+            if (pg1 >= 0) tma_load_2d(st + bx * 16384 + 8192, &tm_k, &ctl->full[s], x, pg1 * 64);
+          }
         }
       }
       // never leave with copies in flight: wait for the last fill of every stage
@@ -410,67 +480,216 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool any_radix = false;
 #pragma unroll
   for (int tt = 0; tt < T; ++tt) any_radix |= ctl->radix[tt] != 0;
+  // Warp w owns the contiguous segment [w*seg, (w+1)*seg) of this CTA's positions (whole
+  // multiples of 128: a lane reads 4 consecutive keys), so the compaction needs no block barrier.
+  const int seg = ((nscan + kThreads / 32 - 1) / (kThreads / 32) + 127) / 128 * 128;
+  const int e_lo = min(nscan, warp * seg), e_hi = min(nscan, e_lo + seg);
 
+  // First radix pass (the epilogue built its histogram while the keys streamed): every CTA finds
+  // the 11-bit bin that holds the K-th key and how many keys of the cluster fall into it.
+  bool fast = false;
   if (any_radix) {
+    cluster_sync();
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-      const int nbits = pass == 2 ? 10 : 11;
-      const uint32_t bmask = (1u << nbits) - 1u;
-      const uint32_t pmask = pass == 0 ? 0u : (0xffffffffu << (shift + nbits));
-      uint32_t* hb = hist + (pass & 1) * T * kHistWords;
-      if (pass > 0) {  // pass 0 was built by the epilogue while the keys streamed
-        for (int i = tid; i < T * kHistWords; i += kThreads) hb[i] = 0u;
-        __syncthreads();
+    for (int tt = 0; tt < T; ++tt) {
+      if (!ctl->radix[tt]) continue;  // uniform over the block
+      uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (tid < kHistThreads) {
+        const uint32_t* h = hist + tt * kHistWords + 4 * tid;
+        for (int r = 0; r < p.C; ++r) {
+          const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
+          cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
+          cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
+          cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
+          cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
+        }
       }
+      uint32_t sum = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum += cnt[k];
+      if (tid == 0) {
+        ctl->found_bin[tt] = 0;
+        ctl->found_need[tt] = 1;
+        ctl->cand_total[tt] = 0x7fffffff;
+      }
+      const uint32_t above = block_excl_suffix(sum, ctl->scan);
+      const uint32_t need = (uint32_t)ctl->need[tt];
+      uint32_t run = above;
+#pragma unroll
+      for (int k = 7; k >= 0; --k) {
+        if (run < need && run + cnt[k] >= need) {
+          ctl->found_bin[tt] = 8 * tid + k;
+          ctl->found_need[tt] = (int)(need - run);
+          ctl->cand_total[tt] = (int)cnt[k];
+        }
+        run += cnt[k];
+      }
+      __syncthreads();
+      if (tid == 0) {
+        ctl->prefix[tt] = (uint32_t)ctl->found_bin[tt] << 21;
+        ctl->need[tt] = ctl->found_need[tt];
+      }
+      __syncthreads();
+    }
+    // Candidate path when every threshold bin is small enough to gather into one CTA.
+    const int cap = p.nstage * CF::kTileBytes / 2 / 8 / T;
+    fast = true;
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt)
+      if (ctl->radix[tt] && ctl->cand_total[tt] > cap) fast = false;  // uniform over the cluster
+  }
+
+  if (fast) {
+    // ---- candidate path: 2 cluster barriers instead of 4.
+    // (a) per warp segment: keys certainly selected ("sure": above the threshold bin, or every
+    //     visible key of a token that sees fewer than K positions) are counted, keys in the
+    //     threshold bin are written, in ascending position order, to this CTA's candidate list
+    //     in the first half of the (now idle) TMA ring.
+    const int cap = p.nstage * CF::kTileBytes / 2 / 8 / T;
+    uint2* own_list = reinterpret_cast<uint2*>(stage_base);
+    uint2* gath = reinterpret_cast<uint2*>(stage_base + p.nstage * CF::kTileBytes / 2);
+    // a1: count per warp segment
 #pragma unroll 1
-      for (int tt = 0; tt < T && pass > 0; ++tt) {
-        if (!ctl->radix[tt]) continue;
+    for (int tt = 0; tt < T; ++tt) {
+      const bool rdx = ctl->radix[tt] != 0;
+      const uint32_t b0 = ctl->prefix[tt] >> 21;
+      const uint32_t* sc = scores + tt * p.chunk;
+      uint32_t sure = 0, cand = 0;
+#pragma unroll 4
+      for (int e = e_lo + 4 * lane; e < e_hi; e += 128) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sc + e);
+        const uint32_t us[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          sure += rdx ? ((us[k] >> 21) > b0) : (us[k] != 0u);
+          cand += (rdx && us[k] != 0u && (us[k] >> 21) == b0);
+        }
+      }
+      sure = __reduce_add_sync(0xffffffffu, sure);
+      cand = __reduce_add_sync(0xffffffffu, cand);
+      if (lane == 0) {
+        ctl->wgt[tt][warp] = (int)sure;
+        ctl->weq[tt][warp] = (int)cand;  // candidates of the warp (replaced in step d)
+      }
+    }
+    __syncthreads();
+    // a2: write the candidates in ascending position order (warp segments are in order)
+#pragma unroll 1
+    for (int tt = 0; tt < T; ++tt) {
+      if (!ctl->radix[tt]) continue;
+      const uint32_t b0 = ctl->prefix[tt] >> 21;
+      const uint32_t* sc = scores + tt * p.chunk;
+      int run = 0;
+      for (int w = 0; w < warp; ++w) run += ctl->weq[tt][w];
+      uint2* dst = own_list + tt * cap;
+      // batches of four 128-key groups: lane holds keys 4*lane..4*lane+3 of each group
+#pragma unroll 1
+      for (int eb = e_lo; eb < e_hi; eb += 512) {
+        uint32_t key[16];
+        uint32_t fc = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (eb + 128 * g < e_hi) v = *reinterpret_cast<const uint4*>(sc + eb + 128 * g + 4 * lane);
+          key[4 * g + 0] = v.x; key[4 * g + 1] = v.y; key[4 * g + 2] = v.z; key[4 * g + 3] = v.w;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (key[4 * g + k] != 0u && (key[4 * g + k] >> 21) == b0) fc |= 1u << (4 * g + k);
+        }
+        const uint32_t cnt = nibble_counts(fc);
+        const uint32_t inc = warp_incl_scan(cnt);
+        const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31);
+        const uint32_t exc = inc - cnt;
+        int base = run;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          int slot = base + (int)((exc >> (8 * g)) & 0xffu);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if ((fc >> (4 * g + k)) & 1u)
+              dst[slot++] = make_uint2(key[4 * g + k], (uint32_t)(lo + eb + 128 * g + 4 * lane + k));
+          base += (int)((tot >> (8 * g)) & 0xffu);
+        }
+        run = base;
+      }
+    }
+    __syncthreads();
+    if (tid < T) {
+      int g = 0, c = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        g += ctl->wgt[tid][w];
+        c += ctl->weq[tid][w];
+      }
+      ctl->cnt_gt[tid] = g;  // this CTA's sure keys (read by the cluster)
+      ctl->own_cnt[tid] = c;
+    }
+    cluster_sync();
+    // (b) read every rank's sure count and gather every rank's candidates (rank order)
+    if (tid < T * p.C) {
+      const int tt = tid / p.C, r = tid % p.C;
+      ctl->rsure[tt][r] = (int)ld_cluster_u32(map_cluster(&ctl->cnt_gt[tt], (uint32_t)r));
+      ctl->rn[tt][r] = ctl->radix[tt] ? (int)ld_cluster_u32(map_cluster(&ctl->own_cnt[tt], (uint32_t)r)) : 0;
+    }
+    __syncthreads();
+    if (tid < T) {
+      int o = 0;
+      for (int r = 0; r < p.C; ++r) {
+        ctl->roff[tid][r] = o;
+        o += ctl->rn[tid][r];
+      }
+      ctl->cand_total[tid] = o;  // equals the histogram count unless a score was NaN
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int tt = 0; tt < T; ++tt) {
+      if (!ctl->radix[tt]) continue;
+      const int n = ctl->cand_total[tt];
+      // four loads in flight per thread before their stores
+#pragma unroll 1
+      for (int i0 = tid; i0 < n; i0 += 4 * kThreads) {
+        uint2 v[4];
+        int at[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * kThreads;
+          at[u] = i;
+          if (i < n) {
+            int r = 0;
+            while (r + 1 < p.C && ctl->roff[tt][r + 1] <= i) ++r;
+            v[u] = ld_cluster_v2(map_cluster(own_list + tt * cap + (i - ctl->roff[tt][r]), (uint32_t)r));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (at[u] < n) gath[tt * cap + at[u]] = v[u];
+      }
+    }
+    cluster_arrive();  // this CTA has finished reading the other CTAs' shared memory
+    __syncthreads();
+    // (c) the remaining 21 bits among the gathered candidates, locally (no cluster barrier)
+#pragma unroll 1
+    for (int tt = 0; tt < T; ++tt) {
+      if (!ctl->radix[tt]) continue;
+      const int n = ctl->cand_total[tt];
+      const uint2* G = gath + tt * cap;
+      uint32_t* h = hist + tt * kHistWords;
+#pragma unroll 1
+      for (int pass = 1; pass < 3; ++pass) {
+        const int shift = pass == 1 ? 10 : 0;
+        const uint32_t bmask = pass == 1 ? 2047u : 1023u;
         const uint32_t pref = ctl->prefix[tt];
-        const uint32_t* sc = scores + tt * p.chunk;
-        uint32_t* h = hb + tt * kHistWords;
-        for (int e = tid; e < nscan; e += kThreads) {
-          const uint32_t u = sc[e];
-          if (u != 0u && (u & pmask) == pref) {
+        const uint32_t pmask = pass == 1 ? 0xffe00000u : 0xfffffc00u;
+        for (int i = tid; i < kHistWords; i += kThreads) h[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t u = G[i].x;
+          if ((u & pmask) == pref) {
             const uint32_t bin = (u >> shift) & bmask;
             atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
           }
         }
-      }
-      cluster_sync();
-#pragma unroll 1
-      for (int tt = 0; tt < T; ++tt) {
-        if (!ctl->radix[tt]) continue;  // uniform over the block
-        uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (tid < kHistThreads) {
-          const uint32_t* h = hb + tt * kHistWords + 4 * tid;
-          for (int r = 0; r < p.C; ++r) {
-            const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
-            cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
-            cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
-            cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
-            cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
-          }
-        }
-        uint32_t sum = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sum += cnt[k];
-        if (tid == 0) {  // defaults, overwritten by the one thread whose bins hold the K-th key
-          ctl->found_bin[tt] = 0;
-          ctl->found_need[tt] = 1;
-        }
-        const uint32_t above = block_excl_suffix(sum, ctl->scan);
-        const uint32_t need = (uint32_t)ctl->need[tt];
-        uint32_t run = above;
-#pragma unroll
-        for (int k = 7; k >= 0; --k) {
-          if (run < need && run + cnt[k] >= need) {
-            ctl->found_bin[tt] = 8 * tid + k;
-            ctl->found_need[tt] = (int)(need - run);
-          }
-          run += cnt[k];
-        }
         __syncthreads();
+        find_bin_local(h, (uint32_t)ctl->need[tt], tt, ctl);
         if (tid == 0) {
           ctl->prefix[tt] |= (uint32_t)ctl->found_bin[tt] << shift;
           ctl->need[tt] = ctl->found_need[tt];
@@ -478,59 +697,211 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
       }
     }
-  }
-
-  // Counts above / at the threshold.  Warp w owns the contiguous segment [w*seg, (w+1)*seg) of
-  // this CTA's positions, so the compaction below needs no block-wide barrier.
-  const int seg = ((nscan + kThreads / 32 - 1) / (kThreads / 32) + 31) / 32 * 32;
-  const int e_lo = warp * seg, e_hi = min(nscan, e_lo + seg);
+    // (d) candidates above / at the threshold per rank, and per warp of this CTA.  The gathered
+    //     list is in (rank, position) order, so runs of equal owners aggregate within a warp.
+    if (tid < T * p.C) {
+      ctl->rgt[tid / p.C][tid % p.C] = 0;
+      ctl->req[tid / p.C][tid % p.C] = 0;
+    }
+    if (tid < T * (kThreads / 32)) {
+      const int tt = tid / (kThreads / 32), w = tid % (kThreads / 32);
+      if (ctl->radix[tt]) ctl->weq[tt][w] = 0;
+    }
+    __syncthreads();
 #pragma unroll 1
-  for (int tt = 0; tt < T; ++tt) {
-    const uint32_t thr = ctl->radix[tt] ? ctl->prefix[tt] : 0u;
-    const uint32_t* sc = scores + tt * p.chunk;
-    uint32_t gt = 0, eq = 0;
-    for (int e = e_lo + lane; e < e_hi; e += 32) {
-      const uint32_t u = sc[e];
-      gt += u > thr;
-      eq += (u == thr && u != 0u);
+    for (int tt = 0; tt < T; ++tt) {
+      if (!ctl->radix[tt]) continue;
+      const int n = ctl->cand_total[tt];
+      const uint2* G = gath + tt * cap;
+      const uint32_t thr = ctl->prefix[tt];
+      // Owner bucket of a candidate: its rank, or kMaxCluster + warp for this CTA's own keys.
+      // Buckets are contiguous runs of the list; a lane walks its share in index order and
+      // flushes its counts when the bucket changes.
+      auto flush = [&](int bk, int ng, int ne) {
+        if (bk < 0 || (ng == 0 && ne == 0)) return;
+        const int r = bk < kMaxCluster ? bk : rank;
+        if (ng) atomicAdd(&ctl->rgt[tt][r], ng);
+        if (ne) atomicAdd(&ctl->req[tt][r], ne);
+        if (bk >= kMaxCluster) {
+          if (ng) atomicAdd(&ctl->wgt[tt][bk - kMaxCluster], ng);
+          if (ne) atomicAdd(&ctl->weq[tt][bk - kMaxCluster], ne);
+        }
+      };
+      const int span = ((n + kThreads / 32 - 1) / (kThreads / 32) + 31) / 32 * 32;
+      const int i_end = min(n, warp * span + span);
+      int cur = -1, ng = 0, ne = 0;
+      bool split = false;
+      for (int i = warp * span + lane; i < i_end; i += 32) {
+        const uint2 c = G[i];
+        const int r = (int)c.y / p.chunk;
+        const int bk = r == rank ? kMaxCluster + ((int)c.y - lo) / seg : r;
+        if (bk != cur) {
+          if (cur >= 0) {
+            flush(cur, ng, ne);
+            split = true;
+          }
+          cur = bk;
+          ng = ne = 0;
+        }
+        ng += c.x > thr;
+        ne += c.x == thr;
+      }
+      // usual case: the whole warp saw one bucket -> one reduction and one atomic per counter
+      const int lead = __shfl_sync(0xffffffffu, cur, 0);
+      if (__all_sync(0xffffffffu, !split && (cur == lead || cur < 0))) {
+        const int sg = (int)__reduce_add_sync(0xffffffffu, (uint32_t)ng);
+        const int se = (int)__reduce_add_sync(0xffffffffu, (uint32_t)ne);
+        if (lane == 0) flush(lead, sg, se);
+      } else {
+        flush(cur, ng, ne);
+      }
     }
-    gt = __reduce_add_sync(0xffffffffu, gt);
-    eq = __reduce_add_sync(0xffffffffu, eq);
-    if (lane == 0) {
-      ctl->wgt[tt][warp] = (int)gt;
-      ctl->weq[tt][warp] = (int)eq;
+    __syncthreads();
+    if (tid < T) {
+      const int tt = tid;
+      const int need_eq = ctl->radix[tt] ? ctl->need[tt] : 0;
+      int eq_before = 0, off = 0, my_quota = 0;
+      for (int r = 0; r < p.C; ++r) {
+        const int gt_r = ctl->rsure[tt][r] + ctl->rgt[tt][r];
+        const int eq_r = ctl->req[tt][r];
+        const int quota_r = max(0, min(eq_r, need_eq - eq_before));
+        if (r < rank) off += gt_r + quota_r;
+        if (r == rank) my_quota = quota_r;
+        eq_before += eq_r;
+      }
+      ctl->offset[tt] = off;
+      ctl->quota[tt] = my_quota;
     }
+    __syncthreads();
+  } else {
+    // ---- general path: radix passes 2 and 3 over every key, cluster-wide
+    if (any_radix) {
+#pragma unroll 1
+      for (int pass = 1; pass < 3; ++pass) {
+        const int shift = pass == 1 ? 10 : 0;
+        const int nbits = pass == 2 ? 10 : 11;
+        const uint32_t bmask = (1u << nbits) - 1u;
+        const uint32_t pmask = 0xffffffffu << (shift + nbits);
+        uint32_t* hb = hist + (pass & 1) * T * kHistWords;
+        for (int i = tid; i < T * kHistWords; i += kThreads) hb[i] = 0u;
+        __syncthreads();
+#pragma unroll 1
+        for (int tt = 0; tt < T; ++tt) {
+          if (!ctl->radix[tt]) continue;
+          const uint32_t pref = ctl->prefix[tt];
+          const uint4* sc4 = reinterpret_cast<const uint4*>(scores + tt * p.chunk);
+          uint32_t* h = hb + tt * kHistWords;
+#pragma unroll 4
+          for (int e4 = tid; e4 < nscan / 4; e4 += kThreads) {
+            const uint4 v = sc4[e4];
+            const uint32_t us[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t u = us[k];
+              if (u != 0u && (u & pmask) == pref) {
+                const uint32_t bin = (u >> shift) & bmask;
+                atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
+              }
+            }
+          }
+        }
+        cluster_sync();
+#pragma unroll 1
+        for (int tt = 0; tt < T; ++tt) {
+          if (!ctl->radix[tt]) continue;  // uniform over the block
+          uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          if (tid < kHistThreads) {
+            const uint32_t* h = hb + tt * kHistWords + 4 * tid;
+            for (int r = 0; r < p.C; ++r) {
+              const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
+              cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
+              cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
+              cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
+              cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
+            }
+          }
+          uint32_t sum = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sum += cnt[k];
+          if (tid == 0) {
+            ctl->found_bin[tt] = 0;
+            ctl->found_need[tt] = 1;
+          }
+          const uint32_t above = block_excl_suffix(sum, ctl->scan);
+          const uint32_t need = (uint32_t)ctl->need[tt];
+          uint32_t run = above;
+#pragma unroll
+          for (int k = 7; k >= 0; --k) {
+            if (run < need && run + cnt[k] >= need) {
+              ctl->found_bin[tt] = 8 * tid + k;
+              ctl->found_need[tt] = (int)(need - run);
+            }
+            run += cnt[k];
+          }
+          __syncthreads();
+          if (tid == 0) {
+            ctl->prefix[tt] |= (uint32_t)ctl->found_bin[tt] << shift;
+            ctl->need[tt] = ctl->found_need[tt];
+          }
+          __syncthreads();
+        }
+      }
+    }
+    // counts above / at the threshold, per warp segment and per CTA
+#pragma unroll 1
+    for (int tt = 0; tt < T; ++tt) {
+      const uint32_t thr = ctl->radix[tt] ? ctl->prefix[tt] : 0u;
+      const uint32_t* sc = scores + tt * p.chunk;
+      uint32_t gt = 0, eq = 0;
+#pragma unroll 4
+      for (int e = e_lo + 4 * lane; e < e_hi; e += 128) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sc + e);
+        const uint32_t us[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          gt += us[k] > thr;
+          eq += (us[k] == thr && us[k] != 0u);
+        }
+      }
+      gt = __reduce_add_sync(0xffffffffu, gt);
+      eq = __reduce_add_sync(0xffffffffu, eq);
+      if (lane == 0) {
+        ctl->wgt[tt][warp] = (int)gt;
+        ctl->weq[tt][warp] = (int)eq;
+      }
+    }
+    __syncthreads();
+    if (tid < T) {
+      int g = 0, q = 0;
+      for (int w = 0; w < kThreads / 32; ++w) {
+        g += ctl->wgt[tid][w];
+        q += ctl->weq[tid][w];
+      }
+      ctl->cnt_gt[tid] = g;
+      ctl->cnt_eq[tid] = q;
+    }
+    cluster_sync();
+    if (tid < T) {
+      const int tt = tid;
+      const int need_eq = ctl->radix[tt] ? ctl->need[tt] : 0;
+      int eq_before = 0, off = 0, my_quota = 0;
+      for (int r = 0; r < p.C; ++r) {
+        const int gt_r = (int)ld_cluster_u32(map_cluster(&ctl->cnt_gt[tt], (uint32_t)r));
+        const int eq_r = (int)ld_cluster_u32(map_cluster(&ctl->cnt_eq[tt], (uint32_t)r));
+        const int quota_r = max(0, min(eq_r, need_eq - eq_before));
+        if (r < rank) off += gt_r + quota_r;
+        if (r == rank) my_quota = quota_r;
+        eq_before += eq_r;
+      }
+      ctl->offset[tt] = off;
+      ctl->quota[tt] = my_quota;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  if (tid < T) {
-    int g = 0, q = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
-      g += ctl->wgt[tid][w];
-      q += ctl->weq[tid][w];
-    }
-    ctl->cnt_gt[tid] = g;
-    ctl->cnt_eq[tid] = q;
-  }
-  cluster_sync();
-  if (tid < T) {
-    const int tt = tid;
-    const int need_eq = ctl->radix[tt] ? ctl->need[tt] : 0;
-    int eq_before = 0, off = 0, my_quota = 0;
-    for (int r = 0; r < p.C; ++r) {
-      const int gt_r = (int)ld_cluster_u32(map_cluster(&ctl->cnt_gt[tt], (uint32_t)r));
-      const int eq_r = (int)ld_cluster_u32(map_cluster(&ctl->cnt_eq[tt], (uint32_t)r));
-      const int quota_r = max(0, min(eq_r, need_eq - eq_before));
-      if (r < rank) off += gt_r + quota_r;
-      if (r == rank) my_quota = quota_r;
-      eq_before += eq_r;
-    }
-    ctl->offset[tt] = off;
-    ctl->quota[tt] = my_quota;
-  }
-  __syncthreads();
 
-  // ascending-position compaction: ties at the threshold go to the lowest positions
-  const uint32_t lt_mask = (1u << lane) - 1u;
+  // ascending-position compaction: ties at the threshold go to the lowest positions.  A warp
+  // stages its selected positions in place at the front of its own segment of the key array
+  // (never ahead of what it has read), then writes them out with coalesced stores.
 #pragma unroll 1
   for (int tt = 0; tt < nt; ++tt) {
     const bool radix = ctl->radix[tt] != 0;
@@ -544,32 +915,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int my_ties = max(0, min(ctl->weq[tt][warp], ctl->quota[tt] - eq_before));
     int* out = p.out_idx + (size_t)(t0 + tt) * p.K;
-    const uint32_t* sc = scores + tt * p.chunk;
-    int eq_run = 0, sel_run = off;
-    for (int e0 = e_lo; e0 < e_hi; e0 += 32) {
-      const int e = e0 + lane;
-      const uint32_t u = e < e_hi ? sc[e] : 0u;
-      const bool f_eq = radix && u == thr && u != 0u;
-      const uint32_t meq = __ballot_sync(0xffffffffu, f_eq);
-      const bool take = (u > thr) || (f_eq && eq_run + __popc(meq & lt_mask) < my_ties);
-      const uint32_t mt = __ballot_sync(0xffffffffu, take);
-      if (take) {
-        const int slot = sel_run + __popc(mt & lt_mask);
-        if (slot < need_total)
-          out[slot] = lo + e;
-        else
-          report(p.status, kStatusDeviceCheck);
+    uint32_t* sc = scores + tt * p.chunk;
+    int eq_run = 0, sel_run = 0;
+    // batches of four 128-key groups: lane holds keys 4*lane..4*lane+3 of each group
+#pragma unroll 1
+    for (int eb = e_lo; eb < e_hi; eb += 512) {
+      uint32_t key[16];
+      uint32_t take = 0, feq = 0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (eb + 128 * g < e_hi) v = *reinterpret_cast<const uint4*>(sc + eb + 128 * g + 4 * lane);
+        key[4 * g + 0] = v.x; key[4 * g + 1] = v.y; key[4 * g + 2] = v.z; key[4 * g + 3] = v.w;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t u = key[4 * g + k];
+          if (u > thr) take |= 1u << (4 * g + k);
+          if (radix && u == thr && u != 0u) feq |= 1u << (4 * g + k);
+        }
       }
-      eq_run += __popc(meq);
-      sel_run += __popc(mt);
+      if (__any_sync(0xffffffffu, feq != 0u)) {
+        // keys equal to the threshold: this warp takes the first my_ties of them
+        const uint32_t ecnt = nibble_counts(feq);
+        const uint32_t einc = warp_incl_scan(ecnt);
+        const uint32_t etot = __shfl_sync(0xffffffffu, einc, 31);
+        const uint32_t eexc = einc - ecnt;
+        int ebase = eq_run;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          int seen = ebase + (int)((eexc >> (8 * g)) & 0xffu);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if ((feq >> (4 * g + k)) & 1u) {
+              if (seen < my_ties) take |= 1u << (4 * g + k);
+              ++seen;
+            }
+          ebase += (int)((etot >> (8 * g)) & 0xffu);
+        }
+        eq_run = ebase;
+      }
+      const uint32_t tcnt = nibble_counts(take);
+      const uint32_t tinc = warp_incl_scan(tcnt);
+      const uint32_t ttot = __shfl_sync(0xffffffffu, tinc, 31);
+      const uint32_t texc = tinc - tcnt;
+      // every lane's keys of the batch are in registers (the scan above), and the staged count
+      // never exceeds the keys read so far: the writes land on keys already consumed
+      int base = sel_run;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if ((take >> (4 * g + k)) & 1u) sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
+        base += (int)((ttot >> (8 * g)) & 0xffu);
+      }
+      sel_run = base;
+    }
+    __syncwarp();
+    for (int j = lane; j < sel_run; j += 32) {
+      if (off + j < need_total)
+        out[off + j] = (int)sc[e_lo + j];
+      else
+        report(p.status, kStatusDeviceCheck);
     }
     if (rank == 0) {
       for (int r = need_total + tid; r < p.K; r += kThreads) out[r] = -1;
       if (tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_total;
     }
   }
-  // peers may still be reading this CTA's counters
-  cluster_sync();
+  // peers may still be reading this CTA's counters / candidates
+  if (fast)
+    cluster_wait();
+  else
+    cluster_sync();
 }
 
 // ---------------------------------------------------------------- host side

@@ -115,6 +115,21 @@ DSA_DEV void prefetch_tmap(const CUtensorMap* m) {
 }
 
 // 2-D tiled load of one box into shared memory, completing bytes on `bar`.
+// L2 policy for data that is read once: its lines are the first to be replaced, so a stream
+// larger than L2 does not push out code and the small tensors other CTAs still need.
+DSA_DEV uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+DSA_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
 DSA_DEV void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -296,6 +311,13 @@ DSA_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
+// Split cluster barrier: arrive (release) now, wait (acquire) later.
+DSA_DEV void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+DSA_DEV void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Address of the same shared variable in CTA `rank` of the cluster (shared::cluster window).
 DSA_DEV uint32_t map_cluster(const void* local, uint32_t rank) {
   uint32_t r;
@@ -305,6 +327,11 @@ DSA_DEV uint32_t map_cluster(const void* local, uint32_t rank) {
 DSA_DEV uint32_t ld_cluster_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+DSA_DEV uint2 ld_cluster_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
   return v;
 }
 DSA_DEV uint4 ld_cluster_v4(uint32_t addr) {
