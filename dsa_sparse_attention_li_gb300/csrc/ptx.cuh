@@ -90,15 +90,50 @@ DSA_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, with acquire semantics at cluster scope: for phases completed by arrivals
+// of another CTA of the cluster that released its own shared::cluster stores.
+DSA_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster address) without ordering
+// this thread's earlier memory operations: for signals whose only precondition is that values
+// this thread loaded have been consumed (an in-order thread issues the arrive after them).
+DSA_DEV void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Asynchronous 16-byte store into the shared memory of a CTA of the cluster; its completion is
+// counted (16 bytes) on that CTA's mbarrier `remote_bar` (both shared::cluster addresses).
+DSA_DEV void st_async_v4(uint32_t cluster_addr, uint4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1,%2,%3,%4}, [%5];" ::"r"(
+          cluster_addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+      : "memory");
+}
+
 // Bounded wait for phase `parity` of `bar`.  Returns false (and raises *abort) when the limit
 // runs out or another thread of the CTA already aborted.
+template <bool kCluster = false>
 DSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_once = [&]() {
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (try_once()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 4; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (try_once()) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -333,6 +368,11 @@ DSA_DEV uint2 ld_cluster_v2(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared::cluster.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
   return v;
+}
+DSA_DEV void st_cluster_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
 }
 DSA_DEV uint4 ld_cluster_v4(uint32_t addr) {
   uint4 v;

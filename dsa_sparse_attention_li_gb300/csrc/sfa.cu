@@ -11,23 +11,27 @@
 // blocks); "Day0 Inference Adaptation ... CANN", section 3.1 (SFA reads the main attention KV at
 // the indexer's positions).
 //
-// Work decomposition.  A CTA (16 warps) serves one (query token, value half r, row split s):
-//   - Q[t] (128 heads x 576, bf16) is split: dims 0..319 are written into TMEM (they are the A
-//     operand of the first 20 k-steps of Q.K^T), dims 320..575 are staged by TMA into a
-//     128-byte-swizzled K-major shared-memory tile;
+// Work decomposition.  A cluster of two CTAs (16 warps each) serves one (query token t, row
+// split s); CTA r of the pair owns the value columns [256r, 256r + 256) and, for Q.K^T, the
+// head dimensions D_r = [256r, 256r + 256) + [512 + 32r, 512 + 32r + 32) (half of the 576):
+//   - Q[t] restricted to D_r (128 heads x 288, bf16) lives in TMEM as the A operand of all 18
+//     k-steps of the partial product S_r = Q[:, D_r].K[:, D_r]^T;
 //   - the split's selected positions are translated to physical rows (page table) in shared
-//     memory; eight gather warps then copy each 64-row tile with 16-byte cp.async (one row is 72
-//     chunks; empty slots are zero-filled) into a 2-stage ring laid out [box][row][128 B] with the
-//     128-byte swizzle, so the same tile is the K-major B operand of Q.K^T (N = 64 rows,
-//     K = 576) and the MN-major B operand of P.V (K = 64 rows, N = 256);
-//   - S = Q.K^T goes to TMEM; one thread per head (TMEM lane) masks, scales and exponentiates its
-//     row, writes P (bf16) back to TMEM and accumulates the row sum in fp32; the reference
-//     maximum only moves when a tile's maximum exceeds it by more than 2^8, and only then is the
-//     head's O row rescaled in TMEM;
+//     memory; eight gather warps copy, per 64-row tile, only the 640 bytes of each row the CTA
+//     uses (its 512 value bytes and the 128 rope bytes) with 16-byte cp.async (empty slots are
+//     zero-filled) into a 3-stage ring laid out [box][row][128 B] with the 128-byte swizzle, so a
+//     stage is the K-major B operand of Q.K^T (N = 64 rows) and the MN-major B operand of P.V
+//     (K = 64 rows, N = 256);
+//   - the two CTAs exchange their partial S tiles through distributed shared memory (fp32,
+//     mbarrier-signalled), so both hold the same S = S_0 + S_1; one thread per head (TMEM lane)
+//     masks, scales and exponentiates its row, writes P (bf16) back to TMEM and accumulates the
+//     row sum in fp32; the reference maximum only moves when a tile's maximum exceeds it by more
+//     than 2^8, and only then is the head's O row rescaled in TMEM;
 //   - O (128 x 256 fp32 = half of TMEM) accumulates P.V_r across tiles.
-// Each head's 128x512 fp32 O would fill all of TMEM, so the value columns are split over two
-// CTAs (r = 0, 1) that recompute the same S.  With several row splits the partial (o, lse) are
-// written to the caller's workspace and the last CTA of a (token, r) to finish merges them.
+// Each head's 128x512 fp32 O would fill all of TMEM, hence the value split over the pair; the
+// split of the Q.K^T dimensions halves both the gathered bytes and the tensor work of each CTA.
+// With several row splits the partial (o, lse) are written to the caller's workspace and the
+// last CTA of a (token, r) to finish merges them.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
@@ -48,26 +52,23 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kDvHalf = 256;
 constexpr int kNT = 64;            // gathered rows per tile (MMA N of Q.K^T)
-constexpr int kStages = 2;
-constexpr int kBoxes = kDqk / 64;  // 9 column boxes of 64 bf16 (128 B)
+constexpr int kStages = 3;
+constexpr int kTileBoxes = 5;      // 4 value boxes of 64 columns + the rope box
 constexpr int kBoxBytes = kNT * 128;                        // one box of a tile: 8 KiB
-constexpr int kChunks = kNT * kDqk * 2 / 16;                // 16-byte chunks per tile (4608)
-// Q[t] is split: dims [0, kQTmemDims) live in TMEM (A operand of the first k-steps), the rest in
-// shared memory, so that two 72 KiB gather stages fit beside it.
-constexpr int kQTmemDims = 320;
-constexpr int kQSmemBox0 = kQTmemDims / 64;                 // first shared-memory box (5)
-constexpr int kQSmemBoxes = kBoxes - kQSmemBox0;            // 4
-constexpr int kQBytes = kHeads * kQSmemBoxes * 128;         // 65536
-constexpr int kTileBytes = kNT * kDqk * 2;                  // 73728
+constexpr int kTileBytes = kTileBoxes * kBoxBytes;          // 40 KiB
+constexpr int kRowChunks = kTileBoxes * 8;                  // 16-byte chunks gathered per row (40)
+constexpr int kChunks = kNT * kRowChunks;                   // per tile (2560)
+constexpr int kQKSteps = 18;       // 16 value k-steps + 2 rope k-steps of this CTA
 constexpr int kMaxRows = 2048;     // row slots per CTA
 constexpr float kRescaleLog2 = 8.0f;
 // TMEM columns (512 in total)
-constexpr uint32_t kColS = 0;      // S: 64 columns
+constexpr uint32_t kColS = 0;      // partial S: 64 columns
 constexpr uint32_t kColP = 64;     // P: 64 bf16 per lane = 32 columns
-constexpr uint32_t kColQ = 96;     // Q dims [0, 320): 160 columns (96..255)
+constexpr uint32_t kColQ = 96;     // Q[:, D_r]: 288 bf16 per lane = 144 columns (96..239)
 constexpr uint32_t kColO = 256;    // O half: 256 columns
 constexpr uint32_t kTmemCols = 512;
 static_assert(kChunks % kGatherThreads == 0, "gather split");
+static_assert(kColQ + kQKSteps * 8 <= kColO, "TMEM columns");
 
 struct Params {
   int B, n_q, H, K, max_pages, num_pages;
@@ -88,10 +89,13 @@ struct Params {
   const __nv_bfloat16* kv;
 };
 
+// Shared memory.  The exchange buffers first hold the TMA-staged value columns of Q[:, D_r]
+// (4 boxes of 128 heads x 128 B), which the softmax warps move into TMEM before the first
+// exchange.
 struct Layout {
-  static constexpr int q = 0;
-  static constexpr int stages = q + kQBytes;
-  static constexpr int rows = stages + kStages * kTileBytes;
+  static constexpr int stages = 0;
+  static constexpr int xbuf = stages + kStages * kTileBytes;  // [2][16][128] x 16 B: partial S
+  static constexpr int rows = xbuf + 2 * 16 * kHeads * 16;
   static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
   static constexpr int ctl = masks + kMaxRows / 8;
   static constexpr int total = ctl + 512;
@@ -101,11 +105,13 @@ struct Ctl {
   uint64_t qbar, q_tmem;
   uint64_t full[kStages], empty[kStages];
   uint64_t s_full, s_free, p_full, pv_done, drain;
+  uint64_t xfull[2];  // the peer has written its partial S into this CTA's buffer
+  uint64_t xfree[2];  // the peer has consumed this CTA's previous write into its buffer
   uint32_t tmem_base;
   int abort;
   int last;  // this CTA merges the splits
   int nvalid;
-  int gather_go[3];  // poller's verdict per step (read by all gather threads after bar.sync)
+  int gather_go[2];  // poller's verdict per step (read by all gather threads after bar.sync)
 };
 
 DSA_DEV int find_seq(const int* q_start, int B, int t) {
@@ -135,10 +141,6 @@ DSA_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
-// Asynchronous L2 prefetch of `bytes` (a multiple of 16) starting at a 16-byte aligned address.
-DSA_DEV void l2_prefetch_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 DSA_DEV void cp_async_arrive_noinc(uint64_t* bar) {
@@ -146,22 +148,28 @@ DSA_DEV void cp_async_arrive_noinc(uint64_t* bar) {
                : "memory");
 }
 
+// Byte offset, within a gathered row, of 16-byte chunk ch (< kRowChunks) of value half r.
+DSA_DEV int row_chunk_offset(int ch, int r) {
+  return ch < 32 ? r * (kDvHalf * 2) + ch * 16 : kDv * 2 + (ch - 32) * 16;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* q_s = smem + Layout::q;
   uint8_t* st_s = smem + Layout::stages;
+  uint4* xbuf = reinterpret_cast<uint4*>(smem + Layout::xbuf);
   int* rows_s = reinterpret_cast<int*>(smem + Layout::rows);
   uint32_t* masks_s = reinterpret_cast<uint32_t*>(smem + Layout::masks);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + Layout::ctl);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x % p.splits;
-  const int half = (blockIdx.x / p.splits) & 1;
-  const int t = blockIdx.x / (2 * p.splits);
-  if (t >= p.n_q) return;
+  const int half = blockIdx.x & 1;  // == rank in the cluster pair
+  const int split = (blockIdx.x >> 1) % p.splits;
+  const int t = (blockIdx.x >> 1) / p.splits;
+  if (t >= p.n_q) return;  // uniform over the pair
+  const uint32_t peer = (uint32_t)(half ^ 1);
   const int b = find_seq(p.q_start, p.B, t);
   const int L = p.seq_lens[b];
   const int slot0 = split * p.rows_per;
@@ -179,6 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->drain, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctl->xfull[x], 1);  // one local expect_tx arrival + the peer's stored bytes
+      mbar_init(&ctl->xfree[x], 128);
+    }
     ctl->abort = 0;
     ctl->nvalid = 0;
     fence_barrier_init();
@@ -188,45 +200,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   __syncthreads();  // barriers initialised
+  cluster_sync();   // ... in both CTAs of the pair before any remote arrive
   if (warp == kMmaWarp && lane == 0 && nslot > 0) {
-    // Q boxes 5..8 stay in q_s (A operand); boxes 0..4 land in the (still empty) gather ring and
-    // are moved into TMEM by the softmax warps.  Issued before the row translation below so the
-    // load overlaps it.
+    // value columns of Q[:, D_r] -> the exchange buffers (moved into TMEM by the softmax warps);
+    // issued before the row translation below so the load overlaps it
     prefetch_tmap(&tm_q);
-    mbar_arrive_expect_tx(&ctl->qbar, kQBytes + kQSmemBox0 * kHeads * 128);
-    for (int bx = 0; bx < kQSmemBoxes; ++bx)
-      tma_load_2d(q_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, (kQSmemBox0 + bx) * 64, t * p.H);
-    for (int bx = 0; bx < kQSmemBox0; ++bx)
-      tma_load_2d(st_s + bx * (kHeads * 128), &tm_q, &ctl->qbar, bx * 64, t * p.H);
+    mbar_arrive_expect_tx(&ctl->qbar, 4 * kHeads * 128);
+    for (int bx = 0; bx < 4; ++bx)
+      tma_load_2d(reinterpret_cast<uint8_t*>(xbuf) + bx * (kHeads * 128), &tm_q, &ctl->qbar,
+                  (4 * half + bx) * 64, t * p.H);
   }
   // logical position -> physical row of every slot of this split (-1: empty or invalid), and a
   // validity bit per slot (the softmax masks whole tiles from two words, with no per-slot loads)
+  // (all index loads of a thread first, then all page-table loads: two round trips)
   int last_valid = -1;
-  for (int i0 = 0; i0 < kMaxRows; i0 += kThreads) {
-    const int i = i0 + tid;
-    int row = -1;
-    if (i < nslot) {
-      const int j = p.idx[(size_t)t * p.K + slot0 + i];
-      if (j >= 0) {
-        if (j < L) {
-          const int pg = p.page_table[(size_t)b * p.max_pages + (j >> 6)];
-          if (pg >= 0 && pg < p.num_pages)
-            row = pg * 64 + (j & 63);
-          else
+  {
+    constexpr int kPer = kMaxRows / kThreads;
+    int j[kPer], pg[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = u * kThreads + tid;
+      j[u] = i < nslot ? p.idx[(size_t)t * p.K + slot0 + i] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      pg[u] = (j[u] >= 0 && j[u] < L) ? p.page_table[(size_t)b * p.max_pages + (j[u] >> 6)] : -1;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = u * kThreads + tid;
+      int row = -1;
+      if (i < nslot) {
+        if (j[u] >= 0) {
+          if (j[u] < L && pg[u] >= 0 && pg[u] < p.num_pages)
+            row = pg[u] * 64 + (j[u] & 63);
+          else if (half == 0)
             report(p.status, kStatusDeviceCheck);
-        } else {
+        } else if (j[u] < -1 && half == 0) {
           report(p.status, kStatusDeviceCheck);
         }
-      } else if (j < -1) {
-        report(p.status, kStatusDeviceCheck);
+        rows_s[i] = row;
+        if (row >= 0) last_valid = i;
       }
-      rows_s[i] = row;
-      if (row >= 0) last_valid = i;
+      const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
+      if (lane == 0) masks_s[i >> 5] = m;
     }
-    const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
-    if (lane == 0) masks_s[i >> 5] = m;
   }
-  // tiles needed: up to the last valid slot
+  // tiles needed: up to the last valid slot (the same in both CTAs of the pair)
   last_valid = __reduce_max_sync(0xffffffffu, last_valid + 1) - 1;
   if (lane == 0 && last_valid >= 0) atomicMax(&ctl->nvalid, last_valid + 1);
   tc_fence_before();
@@ -241,24 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
 
   if (warp < kGatherThreads / 32) {
-    // ---------------- gather: 16-byte cp.async of the selected latent rows into the ring,
-    // 128-byte swizzled [box][row][128 B] so the tile is a valid tcgen05 operand
+    // ---------------- gather: 16-byte cp.async of this CTA's 640 bytes of each selected row
+    // into the ring, 128-byte swizzled [box][row][128 B] so the tile is a valid tcgen05 operand
     const int g = tid;
     const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.kv);
-    // Warm L2 with the rows of the first tiles while Q is staged.
-    for (int slot = g; slot < min(nslot, 2 * kStages * kNT); slot += kGatherThreads) {
-      const int row = rows_s[slot];
-      if (row >= 0) l2_prefetch_bulk(kv + (size_t)row * (kDqk * 2), kDqk * 2);
-    }
     // One thread polls each barrier; the other gather warps sleep on a hardware barrier and
     // then read the poller's verdict (a slot that is not rewritten before every gather thread
     // has passed the next bar.sync, so all of them leave the loop at the same step).
-    if (ntile > 0) {  // Q dims 0..319 are staged in the ring until they are copied into TMEM
-      if (g == 0) ctl->gather_go[2] = mbar_wait(&ctl->q_tmem, 0, abort, p.status) ? 1 : 0;
-      named_barrier(1, kGatherThreads);
-    }
-    const bool go = ntile == 0 || *reinterpret_cast<volatile int*>(&ctl->gather_go[2]) != 0;
-    for (int i = 0; go && i < ntile; ++i) {
+    for (int i = 0; i < ntile; ++i) {
       const int s = i % kStages;
       if (i >= kStages) {
         if (g == 0)
@@ -268,26 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*reinterpret_cast<volatile int*>(&ctl->gather_go[i & 1]) == 0) break;
       }
       const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
-#pragma unroll 6
+#pragma unroll 5
       for (int k = 0; k < kChunks / kGatherThreads; ++k) {
         const int c = g + k * kGatherThreads;
-        const int r = c / 72, ch = c % 72;
+        const int r = c / kRowChunks, ch = c % kRowChunks;
         const int slot = i * kNT + r;
         const int row = slot < nslot ? rows_s[slot] : -1;
         const uint32_t dst = base + (uint32_t)((ch >> 3) * kBoxBytes + r * 128 +
                                                (((ch & 7) ^ (r & 7)) << 4));
-        const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + ch * 16 : kv;
+        const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + row_chunk_offset(ch, half) : kv;
         cp_async16(dst, src, row >= 0 ? 16u : 0u);
       }
       cp_async_arrive_noinc(&ctl->full[s]);
-      // Warm L2 with the rows of the tile that will reuse this stage, so its copies return at L2
-      // latency once the stage frees (one bulk prefetch per 1152-byte row).
-      const int pf = i + 2 * kStages;
-      if (pf < ntile && g < kNT) {
-        const int slot = pf * kNT + g;
-        const int row = slot < nslot ? rows_s[slot] : -1;
-        if (row >= 0) l2_prefetch_bulk(kv + (size_t)row * (kDqk * 2), kDqk * 2);
-      }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp && lane == 0) {
@@ -296,14 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_pv = idesc_bf16(128, kDvHalf, /*b_mn_major=*/true);
     // Descriptors are built once; a k-step only moves the start address (the 14-bit address
     // field cannot carry: every operand lies below 256 KiB).
-    const uint64_t qa_desc = sdesc_sw128(smem_u32(q_s), 16, 1024);
     const uint64_t st_desc = sdesc_sw128(smem_u32(st_s), 16, 1024);
-    const uint64_t v_desc = sdesc_sw128(smem_u32(st_s) + (uint32_t)(half * 4 * kBoxBytes), kBoxBytes, 1024);
+    const uint64_t v_desc = sdesc_sw128(smem_u32(st_s), kBoxBytes, 1024);
     bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
     ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
     // Issue whichever is ready first: Q.K^T of the next tile (needs its rows and a free S) or
-    // P.V of the oldest tile whose weights are written (needs P).  Blocking on one of them while
-    // the other is ready would serialise gather, softmax and tensor work.
+    // P.V of the oldest tile whose weights are written (needs P).
     int nqk = 0, npv = 0;
     uint64_t t_idle = 0;
     while (ok && npv < ntile) {
@@ -313,18 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tile was written by cp.async (generic proxy); tcgen05.mma reads it (async proxy)
         fence_proxy_async_smem();
         tc_fence_after();
-        const uint64_t sb = st_desc + (uint64_t)(((nqk % kStages) * kTileBytes) >> 4);
-#pragma unroll 4
-        for (int kk = 0; kk < kQTmemDims / 16; ++kk) {  // A = Q dims from TMEM
-          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          mma_f16_ts(tmem + kColS, tmem + kColQ + (uint32_t)kk * 8u, sb + (off >> 4), idesc_qk,
-                     kk > 0 ? 1u : 0u);
-        }
-#pragma unroll 4
-        for (int kk = kQTmemDims / 16; kk < kDqk / 16; ++kk) {  // A = Q dims from shared memory
-          const uint32_t offb = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          const uint32_t offa = (uint32_t)((kk >> 2) - kQSmemBox0) * (kHeads * 128) + (uint32_t)(kk & 3) * 32u;
-          mma_f16_ss(tmem + kColS, qa_desc + (offa >> 4), sb + (offb >> 4), idesc_qk, 1u);
+        const uint32_t sbase = (uint32_t)((nqk % kStages) * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kQKSteps; ++kk) {
+          // k-steps 0..15: the value boxes; 16, 17: this CTA's half of the rope box
+          const uint32_t off = kk < 16 ? (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u
+                                       : 4u * kBoxBytes + (uint32_t)(2 * half + kk - 16) * 32u;
+          mma_f16_ts(tmem + kColS, tmem + kColQ + (uint32_t)kk * 8u, st_desc + ((sbase + off) >> 4),
+                     idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&ctl->s_full);
         ++nqk;
@@ -365,15 +360,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- softmax: one thread per head row (TMEM lane)
     const int qd = warp - kSoftmaxWarp0, h = qd * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    const uint32_t peer_xbuf = map_cluster(xbuf, peer);
+    const uint32_t peer_xfull = map_cluster(&ctl->xfull[0], peer);
+    const uint32_t peer_xfree = map_cluster(&ctl->xfree[0], peer);
     if (ntile > 0) {
-      // Q[t][h][0:320] (staged by TMA, 128-byte swizzled) -> TMEM columns kColQ.. (two bf16 per
-      // 32-bit column); heads >= H are 0
+      // Q[t][h][D_r] -> TMEM columns kColQ.. (two bf16 per 32-bit column); heads >= H are 0.
+      // Value columns from the TMA-staged boxes (128-byte swizzled), rope columns from global.
       const bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
       (void)ok;
 #pragma unroll 1
-      for (int c = 0; c < kQSmemBox0; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        const uint8_t* box = st_s + c * (kHeads * 128) + h * 128;
+        const uint8_t* box = reinterpret_cast<const uint8_t*>(xbuf) + c * (kHeads * 128) + h * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = h < p.H ? *reinterpret_cast<const uint4*>(box + ((v ^ (h & 7)) << 4))
@@ -383,11 +381,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32), r);
         tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32 + 16), r + 16);
       }
+      {
+        uint32_t r[16];
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.H + h) * kDqk + kDv + 32 * half);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 x = h < p.H ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+        }
+        tmem_st_x16(lane_addr + kColQ + 128u, r);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->q_tmem);
+      // this CTA's buffers no longer hold Q: the peer may write its first two partial tiles
+      mbar_arrive_remote_relaxed(peer_xfree);
+      mbar_arrive_remote_relaxed(peer_xfree + 8u);
     }
     for (int i = 0; i < ntile; ++i) {
+      const int x = i & 1;
+      const uint32_t xph = (uint32_t)(i >> 1) & 1u;
       bool ok = mbar_wait(&ctl->s_full, (uint32_t)i & 1u, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -397,15 +410,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&ctl->s_free);
+      // exchange the partial rows: send ours into the peer's buffer x (asynchronous stores that
+      // count their bytes on the peer's xfull[x]), read the peer's from ours.
+      // Layout [x][chunk c of 4 columns][head] x 16 B: a warp's stores and loads are contiguous.
+      if (h == 0) mbar_arrive_expect_tx(&ctl->xfull[x], 16u * kHeads * 16u);
+      ok = mbar_wait<true>(&ctl->xfree[x], xph, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_async_v4(peer_xbuf + (uint32_t)(((x * 16 + c) * kHeads + h) * 16),
+                    make_uint4(sr[4 * c], sr[4 * c + 1], sr[4 * c + 2], sr[4 * c + 3]),
+                    peer_xfull + 8u * (uint32_t)x);
+      ok = mbar_wait<true>(&ctl->xfull[x], xph, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
       float mt = -INFINITY;
       const uint32_t vm0 = masks_s[2 * i], vm1 = masks_s[2 * i + 1];
 #pragma unroll
-      for (int c = 0; c < kNT; ++c) {
-        const bool valid = ((c < 32 ? vm0 : vm1) >> (c & 31)) & 1u;
-        const float z = valid ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-        sr[c] = __float_as_uint(z);
-        mt = fmaxf(mt, z);
+      for (int c = 0; c < 16; ++c) {
+        const uint4 o = xbuf[(x * 16 + c) * kHeads + h];
+        const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int col = 4 * c + k;
+          // S = S_0 + S_1 in the same order in both CTAs
+          const float a = __uint_as_float(sr[col]), pv = __uint_as_float(ov[k]);
+          const float sv = half == 0 ? a + pv : pv + a;
+          const bool valid = ((col < 32 ? vm0 : vm1) >> (col & 31)) & 1u;
+          const float z = valid ? sv * p.scale_log2 : -INFINITY;
+          sr[col] = __float_as_uint(z);
+          mt = fmaxf(mt, z);
+        }
       }
+      mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);  // our buffer x may be rewritten
       if (i >= 1) {
         ok = mbar_wait(&ctl->pv_done, (uint32_t)(i - 1) & 1u, abort, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -508,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // also: no remote access to either CTA's shared memory after this point
   tc_fence_after();
   if (warp == kMmaWarp) {
     __syncwarp();
@@ -748,8 +784,19 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   if (std::getenv("DSA_VERBOSE"))
     std::fprintf(stderr, "[dsa] sfa %s splits=%d rows_per=%d grid=%u smem=%d\n",
                  prefill ? "prefill" : "decode", pl.splits, pl.rows_per, grid, smem);
-  sfa_kernel<<<grid, kThreads, smem, stream>>>(tm_q, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;  // the two value halves of a (token, split)
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, sfa_kernel, tm_q, p);
   if (e != cudaSuccess) return cuda_fail(e, "sfa: launch", err);
   return DSA_OK;
 }
