@@ -52,7 +52,11 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kDvHalf = 256;
 constexpr int kNT = 64;            // gathered rows per tile (MMA N of Q.K^T)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
+constexpr int kXBufs = 1;          // partial-S exchange buffers
+// Q[:, D_r] value columns are staged (64 KiB) in the exchange buffers when they are large
+// enough, else in the last two ring stages (whose first gathers then wait for Q to reach TMEM)
+constexpr bool kQInRing = kXBufs * 32768 < 65536;
 constexpr int kTileBoxes = 5;      // 4 value boxes of 64 columns + the rope box
 constexpr int kBoxBytes = kNT * 128;                        // one box of a tile: 8 KiB
 constexpr int kTileBytes = kTileBoxes * kBoxBytes;          // 40 KiB
@@ -89,13 +93,13 @@ struct Params {
   const __nv_bfloat16* kv;
 };
 
-// Shared memory.  The exchange buffers first hold the TMA-staged value columns of Q[:, D_r]
-// (4 boxes of 128 heads x 128 B), which the softmax warps move into TMEM before the first
-// exchange.
+// Shared memory.  The TMA-staged value columns of Q[:, D_r] (4 boxes of 128 heads x 128 B) are
+// moved into TMEM by the softmax warps before the region is reused.
 struct Layout {
   static constexpr int stages = 0;
-  static constexpr int xbuf = stages + kStages * kTileBytes;  // [2][16][128] x 16 B: partial S
-  static constexpr int rows = xbuf + 2 * 16 * kHeads * 16;
+  static constexpr int xbuf = stages + kStages * kTileBytes;  // [kXBufs][16][128] x 16 B
+  static constexpr int rows = xbuf + kXBufs * 16 * kHeads * 16;
+  static constexpr int qstage = kQInRing ? stages + (kStages - 2) * kTileBytes : xbuf;
   static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
   static constexpr int ctl = masks + kMaxRows / 8;
   static constexpr int total = ctl + 512;
@@ -105,8 +109,8 @@ struct Ctl {
   uint64_t qbar, q_tmem;
   uint64_t full[kStages], empty[kStages];
   uint64_t s_full, s_free, p_full, pv_done, drain;
-  uint64_t xfull[2];  // the peer has written its partial S into this CTA's buffer
-  uint64_t xfree[2];  // the peer has consumed this CTA's previous write into its buffer
+  uint64_t xfull[kXBufs];  // the peer has written its partial S into this CTA's buffer
+  uint64_t xfree[kXBufs];  // the peer has consumed this CTA's previous write into its buffer
   uint32_t tmem_base;
   int abort;
   int last;  // this CTA merges the splits
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->drain, 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kXBufs; ++x) {
       mbar_init(&ctl->xfull[x], 1);  // one local expect_tx arrival + the peer's stored bytes
       mbar_init(&ctl->xfree[x], 128);
     }
@@ -202,12 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();  // barriers initialised
   cluster_sync();   // ... in both CTAs of the pair before any remote arrive
   if (warp == kMmaWarp && lane == 0 && nslot > 0) {
-    // value columns of Q[:, D_r] -> the exchange buffers (moved into TMEM by the softmax warps);
+    // value columns of Q[:, D_r] -> shared memory (moved into TMEM by the softmax warps);
     // issued before the row translation below so the load overlaps it
     prefetch_tmap(&tm_q);
     mbar_arrive_expect_tx(&ctl->qbar, 4 * kHeads * 128);
     for (int bx = 0; bx < 4; ++bx)
-      tma_load_2d(reinterpret_cast<uint8_t*>(xbuf) + bx * (kHeads * 128), &tm_q, &ctl->qbar,
+      tma_load_2d(smem + Layout::qstage + bx * (kHeads * 128), &tm_q, &ctl->qbar,
                   (4 * half + bx) * 64, t * p.H);
   }
   // logical position -> physical row of every slot of this split (-1: empty or invalid), and a
@@ -269,10 +273,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // has passed the next bar.sync, so all of them leave the loop at the same step).
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kStages;
-      if (i >= kStages) {
+      if (i >= kStages || (kQInRing && i >= kStages - 2)) {
+        // a reused stage waits for the P.V that read it; a stage holding Q waits for TMEM
         if (g == 0)
           ctl->gather_go[i & 1] =
-              mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status) ? 1 : 0;
+              (i >= kStages
+                   ? mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status)
+                   : mbar_wait(&ctl->q_tmem, 0, abort, p.status))
+                  ? 1
+                  : 0;
         named_barrier(1, kGatherThreads);
         if (*reinterpret_cast<volatile int*>(&ctl->gather_go[i & 1]) == 0) break;
       }
@@ -371,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        const uint8_t* box = reinterpret_cast<const uint8_t*>(xbuf) + c * (kHeads * 128) + h * 128;
+        const uint8_t* box = smem + Layout::qstage + c * (kHeads * 128) + h * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = h < p.H ? *reinterpret_cast<const uint4*>(box + ((v ^ (h & 7)) << 4))
@@ -394,13 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->q_tmem);
-      // this CTA's buffers no longer hold Q: the peer may write its first two partial tiles
-      mbar_arrive_remote_relaxed(peer_xfree);
-      mbar_arrive_remote_relaxed(peer_xfree + 8u);
+      // this CTA's buffers are free (Q has left them): the peer may write its first tiles
+#pragma unroll
+      for (int x = 0; x < kXBufs; ++x) mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);
     }
     for (int i = 0; i < ntile; ++i) {
-      const int x = i & 1;
-      const uint32_t xph = (uint32_t)(i >> 1) & 1u;
+      const int x = i % kXBufs;
+      const uint32_t xph = (uint32_t)(i / kXBufs) & 1u;
       bool ok = mbar_wait(&ctl->s_full, (uint32_t)i & 1u, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
