@@ -268,6 +268,17 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 // Shared-memory matrix descriptor, 128-byte swizzle.  K-major operands: rows of 128 B, 8-row
 // groups 1024 B apart (sbo = 1024).  MN-major operands: lbo = distance between 64-element column
 // blocks, sbo = distance between 8-row groups along K.
+// K-major operand with 64-byte rows, 64-byte swizzle (16-byte chunk c of row r stored at chunk
+// c ^ ((r >> 1) & 3)); 8-row groups are sbo (512) bytes apart.
+DSA_DEV uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;  // leading byte offset: unused for swizzled K-major
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;  // 64-byte swizzle
+  return d;
+}
 DSA_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);

@@ -43,8 +43,9 @@
 namespace dsa {
 namespace sfa {
 
-constexpr int kThreads = 512;      // 16 warps: 0-7 gather, 8 MMA, 12-15 softmax
-constexpr int kGatherThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 0-3, 9-11 gather; 4-7 score exchange; 8 MMA; 12-15 softmax
+constexpr int kGatherThreads = 224;
+constexpr int kXchgWarp0 = 4;
 constexpr int kMmaWarp = 8;
 constexpr int kSoftmaxWarp0 = 12;
 constexpr int kHeads = 128;        // MMA M (heads are padded to 128)
@@ -57,22 +58,21 @@ constexpr int kXBufs = 1;          // partial-S exchange buffers
 // Q[:, D_r] value columns are staged (64 KiB) in the exchange buffers when they are large
 // enough, else in the last two ring stages (whose first gathers then wait for Q to reach TMEM)
 constexpr bool kQInRing = kXBufs * 32768 < 65536;
-constexpr int kTileBoxes = 5;      // 4 value boxes of 64 columns + the rope box
-constexpr int kBoxBytes = kNT * 128;                        // one box of a tile: 8 KiB
-constexpr int kTileBytes = kTileBoxes * kBoxBytes;          // 40 KiB
-constexpr int kRowChunks = kTileBoxes * 8;                  // 16-byte chunks gathered per row (40)
-constexpr int kChunks = kNT * kRowChunks;                   // per tile (2560)
-constexpr int kQKSteps = 18;       // 16 value k-steps + 2 rope k-steps of this CTA
+constexpr int kBoxBytes = kNT * 128;                        // one value box of a tile: 8 KiB
+constexpr int kRopeHalf = 32;      // rope columns of this CTA's half of Q.K^T
+constexpr int kRopeBoxBytes = kNT * kRopeHalf * 2;          // 64-byte rows: 4 KiB
+constexpr int kTileBytes = 4 * kBoxBytes + kRopeBoxBytes;   // 36 KiB
+constexpr int kRowChunks = 32 + 4;                          // 16-byte chunks gathered per row
+constexpr int kChunks = kNT * kRowChunks;                   // per tile (2304)
 constexpr int kMaxRows = 2048;     // row slots per CTA
 constexpr float kRescaleLog2 = 8.0f;
 // TMEM columns (512 in total)
-constexpr uint32_t kColS = 0;      // partial S: 64 columns
-constexpr uint32_t kColP = 64;     // P: 64 bf16 per lane = 32 columns
-constexpr uint32_t kColQ = 96;     // Q[:, D_r]: 288 bf16 per lane = 144 columns (96..239)
+constexpr uint32_t kColQ = 0;      // Q value columns of D_r: 256 bf16 per lane = 128 columns
+constexpr uint32_t kColS = 128;    // partial S, two buffers of 64 columns (tile i uses i & 1)
 constexpr uint32_t kColO = 256;    // O half: 256 columns
 constexpr uint32_t kTmemCols = 512;
-static_assert(kChunks % kGatherThreads == 0, "gather split");
-static_assert(kColQ + kQKSteps * 8 <= kColO, "TMEM columns");
+constexpr int kGatherPer = (kChunks + kGatherThreads - 1) / kGatherThreads;  // chunks per thread
+static_assert(kColQ + 128 <= kColS && kColS + 2 * kNT <= kColO, "TMEM columns");
 
 struct Params {
   int B, n_q, H, K, max_pages, num_pages;
@@ -94,11 +94,14 @@ struct Params {
 };
 
 // Shared memory.  The TMA-staged value columns of Q[:, D_r] (4 boxes of 128 heads x 128 B) are
-// moved into TMEM by the softmax warps before the region is reused.
+// moved into TMEM by the softmax warps before the region is reused; the rope columns of Q stay
+// in shared memory (A operand of the two rope k-steps), as does P (A operand of P.V).
 struct Layout {
   static constexpr int stages = 0;
   static constexpr int xbuf = stages + kStages * kTileBytes;  // [kXBufs][16][128] x 16 B
-  static constexpr int rows = xbuf + kXBufs * 16 * kHeads * 16;
+  static constexpr int pbuf = xbuf + kXBufs * 16 * kHeads * 16;  // P: 128 heads x 128 B, SW128
+  static constexpr int qrope = pbuf + kHeads * 128;  // Q rope half: 128 x 64 B, 64-byte swizzle
+  static constexpr int rows = qrope + kHeads * kRopeHalf * 2;
   static constexpr int qstage = kQInRing ? stages + (kStages - 2) * kTileBytes : xbuf;
   static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
   static constexpr int ctl = masks + kMaxRows / 8;
@@ -108,7 +111,7 @@ struct Layout {
 struct Ctl {
   uint64_t qbar, q_tmem;
   uint64_t full[kStages], empty[kStages];
-  uint64_t s_full, s_free, p_full, pv_done, drain;
+  uint64_t s_full[2], s_sum[2], s_free[2], p_full, pv_done, drain;
   uint64_t xfull[kXBufs];  // the peer has written its partial S into this CTA's buffer
   uint64_t xfree[kXBufs];  // the peer has consumed this CTA's previous write into its buffer
   uint32_t tmem_base;
@@ -152,13 +155,21 @@ DSA_DEV void cp_async_arrive_noinc(uint64_t* bar) {
                : "memory");
 }
 
-// Byte offset, within a gathered row, of 16-byte chunk ch (< kRowChunks) of value half r.
+// Byte offset, within a latent row, of 16-byte chunk ch (< kRowChunks) of half r: 32 value
+// chunks, then the 4 chunks of the rope half.
 DSA_DEV int row_chunk_offset(int ch, int r) {
-  return ch < 32 ? r * (kDvHalf * 2) + ch * 16 : kDv * 2 + (ch - 32) * 16;
+  return ch < 32 ? r * (kDvHalf * 2) + ch * 16 : kDv * 2 + r * (kRopeHalf * 2) + (ch - 32) * 16;
+}
+// Shared-memory offset, within a stage, of chunk ch of tile row rr: value chunks go to box ch/8
+// (128-byte swizzle), rope chunks to the rope box (64-byte rows, 64-byte swizzle).
+DSA_DEV uint32_t stage_chunk_offset(int ch, int rr) {
+  return ch < 32 ? (uint32_t)((ch >> 3) * kBoxBytes + rr * 128 + (((ch & 7) ^ (rr & 7)) << 4))
+                 : (uint32_t)(4 * kBoxBytes + rr * 64 + ((((ch - 32) ^ (rr >> 1)) & 3) << 4));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const Params p) {
+    sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
+               const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -186,8 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->full[s], kGatherThreads);
       mbar_init(&ctl->empty[s], 1);
     }
-    mbar_init(&ctl->s_full, 1);
-    mbar_init(&ctl->s_free, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->s_full[b], 1);
+      mbar_init(&ctl->s_sum[b], 128);
+      mbar_init(&ctl->s_free[b], 128);
+    }
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->drain, 1);
@@ -209,10 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // value columns of Q[:, D_r] -> shared memory (moved into TMEM by the softmax warps);
     // issued before the row translation below so the load overlaps it
     prefetch_tmap(&tm_q);
-    mbar_arrive_expect_tx(&ctl->qbar, 4 * kHeads * 128);
+    prefetch_tmap(&tm_qr);
+    mbar_arrive_expect_tx(&ctl->qbar, 4 * kHeads * 128 + kHeads * kRopeHalf * 2);
     for (int bx = 0; bx < 4; ++bx)
       tma_load_2d(smem + Layout::qstage + bx * (kHeads * 128), &tm_q, &ctl->qbar,
                   (4 * half + bx) * 64, t * p.H);
+    tma_load_2d(smem + Layout::qrope, &tm_qr, &ctl->qbar, kDv + kRopeHalf * half, t * p.H);
   }
   // logical position -> physical row of every slot of this split (-1: empty or invalid), and a
   // validity bit per slot (the softmax masks whole tiles from two words, with no per-slot loads)
@@ -263,10 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (normalisation), and the fp32 sum of the unrounded weights (log-sum-exp)
   float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
 
-  if (warp < kGatherThreads / 32) {
+  if (warp < 4 || (warp >= 9 && warp < 12)) {
     // ---------------- gather: 16-byte cp.async of this CTA's 640 bytes of each selected row
     // into the ring, 128-byte swizzled [box][row][128 B] so the tile is a valid tcgen05 operand
-    const int g = tid;
+    const int g = warp < 4 ? tid : tid - 9 * 32 + 128;  // 0 .. kGatherThreads - 1
     const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.kv);
     // One thread polls each barrier; the other gather warps sleep on a hardware barrier and
     // then read the poller's verdict (a slot that is not rewritten before every gather thread
@@ -286,16 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*reinterpret_cast<volatile int*>(&ctl->gather_go[i & 1]) == 0) break;
       }
       const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
-#pragma unroll 5
-      for (int k = 0; k < kChunks / kGatherThreads; ++k) {
+#pragma unroll
+      for (int k = 0; k < kGatherPer; ++k) {
         const int c = g + k * kGatherThreads;
-        const int r = c / kRowChunks, ch = c % kRowChunks;
-        const int slot = i * kNT + r;
-        const int row = slot < nslot ? rows_s[slot] : -1;
-        const uint32_t dst = base + (uint32_t)((ch >> 3) * kBoxBytes + r * 128 +
-                                               (((ch & 7) ^ (r & 7)) << 4));
-        const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + row_chunk_offset(ch, half) : kv;
-        cp_async16(dst, src, row >= 0 ? 16u : 0u);
+        if (c < kChunks) {
+          const int r = c / kRowChunks, ch = c % kRowChunks;
+          const int slot = i * kNT + r;
+          const int row = slot < nslot ? rows_s[slot] : -1;
+          const uint32_t dst = base + stage_chunk_offset(ch, r);
+          const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + row_chunk_offset(ch, half) : kv;
+          cp_async16(dst, src, row >= 0 ? 16u : 0u);
+        }
       }
       cp_async_arrive_noinc(&ctl->full[s]);
     }
@@ -308,29 +325,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // field cannot carry: every operand lies below 256 KiB).
     const uint64_t st_desc = sdesc_sw128(smem_u32(st_s), 16, 1024);
     const uint64_t v_desc = sdesc_sw128(smem_u32(st_s), kBoxBytes, 1024);
+    const uint64_t qr_desc = sdesc_sw64(smem_u32(smem + Layout::qrope), 512);
+    const uint64_t rope_desc = sdesc_sw64(smem_u32(st_s) + 4u * kBoxBytes, 512);
+    const uint64_t p_desc = sdesc_sw128(smem_u32(smem + Layout::pbuf), 16, 1024);
     bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
     ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
-    // Issue whichever is ready first: Q.K^T of the next tile (needs its rows and a free S) or
-    // P.V of the oldest tile whose weights are written (needs P).
+    // Issue whichever is ready first: Q.K^T of the next tile (needs its rows and a free S buffer)
+    // or P.V of the oldest tile whose weights are written (needs P).
     int nqk = 0, npv = 0;
     uint64_t t_idle = 0;
     while (ok && npv < ntile) {
       bool progressed = false;
       if (nqk < ntile && mbar_test(&ctl->full[nqk % kStages], (uint32_t)(nqk / kStages) & 1u) &&
-          (nqk == 0 || mbar_test(&ctl->s_free, (uint32_t)(nqk - 1) & 1u))) {
+          (nqk < 2 || mbar_test(&ctl->s_free[nqk & 1], (uint32_t)((nqk >> 1) - 1) & 1u))) {
         // the tile was written by cp.async (generic proxy); tcgen05.mma reads it (async proxy)
         fence_proxy_async_smem();
         tc_fence_after();
         const uint32_t sbase = (uint32_t)((nqk % kStages) * kTileBytes);
+        const uint32_t d_s = tmem + kColS + (uint32_t)((nqk & 1) * kNT);
 #pragma unroll
-        for (int kk = 0; kk < kQKSteps; ++kk) {
-          // k-steps 0..15: the value boxes; 16, 17: this CTA's half of the rope box
-          const uint32_t off = kk < 16 ? (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u
-                                       : 4u * kBoxBytes + (uint32_t)(2 * half + kk - 16) * 32u;
-          mma_f16_ts(tmem + kColS, tmem + kColQ + (uint32_t)kk * 8u, st_desc + ((sbase + off) >> 4),
-                     idesc_qk, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 16; ++kk) {  // the value boxes, A = Q from TMEM
+          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+          mma_f16_ts(d_s, tmem + kColQ + (uint32_t)kk * 8u, st_desc + ((sbase + off) >> 4), idesc_qk,
+                     kk > 0 ? 1u : 0u);
         }
-        mma_commit(&ctl->s_full);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)  // this CTA's rope half, A = Q from shared memory
+          mma_f16_ss(d_s, qr_desc + (uint64_t)(kk * 2), rope_desc + (uint64_t)((sbase >> 4) + kk * 2),
+                     idesc_qk, 1u);
+        mma_commit(&ctl->s_full[nqk & 1]);
         ++nqk;
         progressed = true;
       }
@@ -340,9 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t vb = v_desc + (uint64_t)((s * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kNT / 16; ++kk) {
-          // B = V rows [16kk, 16kk+16) x this half's 256 value columns, MN-major:
-          // 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024 bytes apart (sbo)
-          mma_f16_ts(tmem + kColO, tmem + kColP + (uint32_t)kk * 8u, vb + (uint64_t)(kk * 2048 >> 4),
+          // A = P (K-major, keys [16kk, 16kk+16)); B = V rows [16kk, 16kk+16) x this half's 256
+          // value columns, MN-major: 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024
+          // bytes apart (sbo)
+          mma_f16_ss(tmem + kColO, p_desc + (uint64_t)(kk * 32 >> 4), vb + (uint64_t)(kk * 2048 >> 4),
                      idesc_pv, (npv > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&ctl->pv_done);
@@ -365,16 +389,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit(&ctl->drain);
     mbar_wait(&ctl->drain, 0, abort, p.status);
-  } else if (warp >= kSoftmaxWarp0) {
-    // ---------------- softmax: one thread per head row (TMEM lane)
-    const int qd = warp - kSoftmaxWarp0, h = qd * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+  } else if (warp >= kXchgWarp0 && warp < kXchgWarp0 + 4) {
+    // ---------------- score exchange: one thread per head row (TMEM lane quadrant warp % 4),
+    // running ahead of the softmax.  The partial row goes into the peer's buffer (asynchronous
+    // stores that count their bytes on the peer's xfull), the peer's partial is added in the same
+    // order in both CTAs (S_0 + S_1), and the sum goes back into the tile's S columns.
+    // Buffer layout [x][chunk c of 4 columns][head] x 16 B: a warp's stores and loads are
+    // contiguous.
+    const int h = (warp - kXchgWarp0) * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp - kXchgWarp0) * 32) << 16);
     const uint32_t peer_xbuf = map_cluster(xbuf, peer);
     const uint32_t peer_xfull = map_cluster(&ctl->xfull[0], peer);
     const uint32_t peer_xfree = map_cluster(&ctl->xfree[0], peer);
     if (ntile > 0) {
-      // Q[t][h][D_r] -> TMEM columns kColQ.. (two bf16 per 32-bit column); heads >= H are 0.
-      // Value columns from the TMA-staged boxes (128-byte swizzled), rope columns from global.
+#pragma unroll
+      for (int x = 0; x < kXBufs; ++x) mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);
+    }
+    for (int i = 0; i < ntile; ++i) {
+      const int x = i % kXBufs;
+      const uint32_t xph = (uint32_t)(i / kXBufs) & 1u;
+      bool ok = mbar_wait(&ctl->s_full[i & 1], (uint32_t)(i >> 1) & 1u, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t sr[64];
+      const uint32_t s_col = kColS + (uint32_t)((i & 1) * kNT);
+      tmem_ld_x32(lane_addr + s_col, sr);
+      tmem_ld_x32(lane_addr + s_col + 32, sr + 32);
+      tmem_ld_wait();
+      if (h == 0) mbar_arrive_expect_tx(&ctl->xfull[x], 16u * kHeads * 16u);
+      ok = mbar_wait<true>(&ctl->xfree[x], xph, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_async_v4(peer_xbuf + (uint32_t)(((x * 16 + c) * kHeads + h) * 16),
+                    make_uint4(sr[4 * c], sr[4 * c + 1], sr[4 * c + 2], sr[4 * c + 3]),
+                    peer_xfull + 8u * (uint32_t)x);
+      ok = mbar_wait<true>(&ctl->xfull[x], xph, abort, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 o = xbuf[(x * 16 + c) * kHeads + h];
+        const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = __uint_as_float(sr[4 * c + k]), b2 = __uint_as_float(ov[k]);
+          sr[4 * c + k] = __float_as_uint(half == 0 ? a + b2 : b2 + a);
+        }
+      }
+      mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);  // our buffer x may be rewritten
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st_x16(lane_addr + s_col + (uint32_t)(16 * c), sr + 16 * c);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&ctl->s_sum[i & 1]);
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ---------------- softmax: one thread per head row (TMEM lane)
+    const int qd = warp - kSoftmaxWarp0, h = qd * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
+    if (ntile > 0) {
+      // Q[t][h][value columns of D_r] -> TMEM columns kColQ.. (two bf16 per 32-bit column) from
+      // the TMA-staged boxes (128-byte swizzled); heads >= H are 0.
       const bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
       (void)ok;
 #pragma unroll 1
@@ -390,67 +465,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32), r);
         tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32 + 16), r + 16);
       }
-      {
-        uint32_t r[16];
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.H + h) * kDqk + kDv + 32 * half);
+      if (h >= p.H) {  // padded heads: zero rope row (the staged rows belong to the next token)
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 x = h < p.H ? src[v] : make_uint4(0u, 0u, 0u, 0u);
-          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
-        }
-        tmem_st_x16(lane_addr + kColQ + 128u, r);
+        for (int v = 0; v < 4; ++v)
+          *reinterpret_cast<uint4*>(smem + Layout::qrope + h * (kRopeHalf * 2) + v * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&ctl->q_tmem);
-      // this CTA's buffers are free (Q has left them): the peer may write its first tiles
-#pragma unroll
-      for (int x = 0; x < kXBufs; ++x) mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);
     }
     for (int i = 0; i < ntile; ++i) {
-      const int x = i % kXBufs;
-      const uint32_t xph = (uint32_t)(i / kXBufs) & 1u;
-      bool ok = mbar_wait(&ctl->s_full, (uint32_t)i & 1u, abort, p.status);
+      // S = S_0 + S_1 of this tile, summed in TMEM by the exchange warps
+      bool ok = mbar_wait(&ctl->s_sum[i & 1], (uint32_t)(i >> 1) & 1u, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld_x32(lane_addr + kColS, sr);
-      tmem_ld_x32(lane_addr + kColS + 32, sr + 32);
+      const uint32_t s_col = kColS + (uint32_t)((i & 1) * kNT);
+      tmem_ld_x32(lane_addr + s_col, sr);
+      tmem_ld_x32(lane_addr + s_col + 32, sr + 32);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&ctl->s_free);
-      // exchange the partial rows: send ours into the peer's buffer x (asynchronous stores that
-      // count their bytes on the peer's xfull[x]), read the peer's from ours.
-      // Layout [x][chunk c of 4 columns][head] x 16 B: a warp's stores and loads are contiguous.
-      if (h == 0) mbar_arrive_expect_tx(&ctl->xfull[x], 16u * kHeads * 16u);
-      ok = mbar_wait<true>(&ctl->xfree[x], xph, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_async_v4(peer_xbuf + (uint32_t)(((x * 16 + c) * kHeads + h) * 16),
-                    make_uint4(sr[4 * c], sr[4 * c + 1], sr[4 * c + 2], sr[4 * c + 3]),
-                    peer_xfull + 8u * (uint32_t)x);
-      ok = mbar_wait<true>(&ctl->xfull[x], xph, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      mbar_arrive(&ctl->s_free[i & 1]);
       float mt = -INFINITY;
       const uint32_t vm0 = masks_s[2 * i], vm1 = masks_s[2 * i + 1];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 o = xbuf[(x * 16 + c) * kHeads + h];
-        const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int col = 4 * c + k;
-          // S = S_0 + S_1 in the same order in both CTAs
-          const float a = __uint_as_float(sr[col]), pv = __uint_as_float(ov[k]);
-          const float sv = half == 0 ? a + pv : pv + a;
-          const bool valid = ((col < 32 ? vm0 : vm1) >> (col & 31)) & 1u;
-          const float z = valid ? sv * p.scale_log2 : -INFINITY;
-          sr[col] = __float_as_uint(z);
-          mt = fmaxf(mt, z);
-        }
+      for (int col = 0; col < kNT; ++col) {
+        const bool valid = ((col < 32 ? vm0 : vm1) >> (col & 31)) & 1u;
+        const float z = valid ? __uint_as_float(sr[col]) * p.scale_log2 : -INFINITY;
+        sr[col] = __float_as_uint(z);
+        mt = fmaxf(mt, z);
       }
-      mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);  // our buffer x may be rewritten
       if (i >= 1) {
         ok = mbar_wait(&ctl->pv_done, (uint32_t)(i - 1) & 1u, abort, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -490,10 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_sum += ls;
       l_exact += le;
-      tmem_st_x16(lane_addr + kColP, pk);
-      tmem_st_x16(lane_addr + kColP + 16, pk + 16);
-      tmem_st_wait();
-      tc_fence_before();
+      // P row h -> shared memory, 128-byte swizzled K-major (the A operand of P.V)
+      uint8_t* prow = smem + Layout::pbuf + h * 128;
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<uint4*>(prow + ((v ^ (h & 7)) << 4)) =
+            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      fence_proxy_async_smem();
       mbar_arrive(&ctl->p_full);
     }
     if (ntile > 0) {
@@ -782,9 +831,12 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "sfa (cuda-core): launch", err);
   }
 
-  CUtensorMap tm_q;
+  CUtensorMap tm_q, tm_qr;
   if (!encode_tmap_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDqk, (uint64_t)a.n_q * a.H,
                       kDqk * 2, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_128B, err))
+    return DSA_ERR_CUDA;
+  if (!encode_tmap_2d(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDqk, (uint64_t)a.n_q * a.H,
+                      kDqk * 2, kRopeHalf, kHeads, CU_TENSOR_MAP_SWIZZLE_64B, err))
     return DSA_ERR_CUDA;
   const int smem = Layout::total + 1024;
   cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -805,7 +857,7 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, sfa_kernel, tm_q, p);
+  e = cudaLaunchKernelEx(&cfg, sfa_kernel, tm_q, tm_qr, p);
   if (e != cudaSuccess) return cuda_fail(e, "sfa: launch", err);
   return DSA_OK;
 }
