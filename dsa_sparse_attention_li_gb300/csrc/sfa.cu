@@ -99,8 +99,8 @@ struct Params {
 struct Layout {
   static constexpr int stages = 0;
   static constexpr int xbuf = stages + kStages * kTileBytes;  // [kXBufs][16][128] x 16 B
-  static constexpr int pbuf = xbuf + kXBufs * 16 * kHeads * 16;  // P: 128 heads x 128 B, SW128
-  static constexpr int qrope = pbuf + kHeads * 128;  // Q rope half: 128 x 64 B, 64-byte swizzle
+  static constexpr int pbuf = xbuf + kXBufs * 16 * kHeads * 16;  // P[2]: 128 heads x 128 B, SW128
+  static constexpr int qrope = pbuf + 2 * kHeads * 128;  // Q rope half: 128 x 64 B, 64-byte swizzle
   static constexpr int rows = qrope + kHeads * kRopeHalf * 2;
   static constexpr int qstage = kQInRing ? stages + (kStages - 2) * kTileBytes : xbuf;
   static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
@@ -111,7 +111,7 @@ struct Layout {
 struct Ctl {
   uint64_t qbar, q_tmem;
   uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[2], s_sum[2], s_free[2], p_full, pv_done, drain;
+  uint64_t s_full[2], s_sum[2], s_free[2], p_full[2], pv_done[2], drain;
   uint64_t xfull[kXBufs];  // the peer has written its partial S into this CTA's buffer
   uint64_t xfree[kXBufs];  // the peer has consumed this CTA's previous write into its buffer
   uint32_t tmem_base;
@@ -201,9 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->s_full[b], 1);
       mbar_init(&ctl->s_sum[b], 128);
       mbar_init(&ctl->s_free[b], 128);
+      mbar_init(&ctl->p_full[b], 128);
+      mbar_init(&ctl->pv_done[b], 1);
     }
-    mbar_init(&ctl->p_full, 128);
-    mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->drain, 1);
     for (int x = 0; x < kXBufs; ++x) {
       mbar_init(&ctl->xfull[x], 1);  // one local expect_tx arrival + the peer's stored bytes
@@ -330,12 +330,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t p_desc = sdesc_sw128(smem_u32(smem + Layout::pbuf), 16, 1024);
     bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
     ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
-    // Issue whichever is ready first: Q.K^T of the next tile (needs its rows and a free S buffer)
-    // or P.V of the oldest tile whose weights are written (needs P).
+    // Issue whichever is ready: P.V of the oldest tile whose weights are written (needs P; it
+    // releases a ring stage) is tested first, then Q.K^T of the next tile (needs its rows and a
+    // free S buffer).
     int nqk = 0, npv = 0;
     uint64_t t_idle = 0;
     while (ok && npv < ntile) {
       bool progressed = false;
+      if (npv < nqk && mbar_test(&ctl->p_full[npv & 1], (uint32_t)(npv >> 1) & 1u)) {
+        tc_fence_after();
+        const int s = npv % kStages;
+        const uint64_t vb = v_desc + (uint64_t)((s * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kNT / 16; ++kk) {
+          // A = P (K-major, keys [16kk, 16kk+16)); B = V rows [16kk, 16kk+16) x this half's 256
+          // value columns, MN-major: 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024
+          // bytes apart (sbo)
+          mma_f16_ss(tmem + kColO, p_desc + (uint64_t)(((npv & 1) * kHeads * 128 + kk * 32) >> 4),
+                     vb + (uint64_t)(kk * 2048 >> 4),
+                     idesc_pv, (npv > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ctl->pv_done[npv & 1]);
+        mma_commit(&ctl->empty[s]);
+        ++npv;
+        progressed = true;
+      }
       if (nqk < ntile && mbar_test(&ctl->full[nqk % kStages], (uint32_t)(nqk / kStages) & 1u) &&
           (nqk < 2 || mbar_test(&ctl->s_free[nqk & 1], (uint32_t)((nqk >> 1) - 1) & 1u))) {
         // the tile was written by cp.async (generic proxy); tcgen05.mma reads it (async proxy)
@@ -355,23 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      idesc_qk, 1u);
         mma_commit(&ctl->s_full[nqk & 1]);
         ++nqk;
-        progressed = true;
-      }
-      if (npv < nqk && mbar_test(&ctl->p_full, (uint32_t)npv & 1u)) {
-        tc_fence_after();
-        const int s = npv % kStages;
-        const uint64_t vb = v_desc + (uint64_t)((s * kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kNT / 16; ++kk) {
-          // A = P (K-major, keys [16kk, 16kk+16)); B = V rows [16kk, 16kk+16) x this half's 256
-          // value columns, MN-major: 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024
-          // bytes apart (sbo)
-          mma_f16_ss(tmem + kColO, p_desc + (uint64_t)(kk * 32 >> 4), vb + (uint64_t)(kk * 2048 >> 4),
-                     idesc_pv, (npv > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&ctl->pv_done);
-        mma_commit(&ctl->empty[s]);
-        ++npv;
         progressed = true;
       }
       if (progressed) {
@@ -497,14 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         sr[col] = __float_as_uint(z);
         mt = fmaxf(mt, z);
       }
-      if (i >= 1) {
-        ok = mbar_wait(&ctl->pv_done, (uint32_t)(i - 1) & 1u, abort, p.status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc_fence_after();
-      }
       // lazy rescale: move the reference maximum only when it is exceeded by more than 2^8
       const bool need = mt > m_ref + kRescaleLog2;
       if (__any_sync(0xffffffffu, need && i >= 1 && l_sum > 0.f)) {
+        // O is rewritten: every P.V so far must have landed
+        ok = mbar_wait(&ctl->pv_done[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u, abort, p.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
         const float alpha = (need && l_sum > 0.f) ? exp2f(m_ref - mt) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < kDvHalf / 32; ++c) {
@@ -536,17 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_sum += ls;
       l_exact += le;
-      // P row h -> shared memory, 128-byte swizzled K-major (the A operand of P.V)
-      uint8_t* prow = smem + Layout::pbuf + h * 128;
+      // P row h -> shared memory buffer i & 1, 128-byte swizzled K-major (the A operand of P.V),
+      // once the P.V that read it two tiles ago has landed
+      if (i >= 2) {
+        ok = mbar_wait(&ctl->pv_done[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort, p.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      uint8_t* prow = smem + Layout::pbuf + (i & 1) * (kHeads * 128) + h * 128;
 #pragma unroll
       for (int v = 0; v < 8; ++v)
         *reinterpret_cast<uint4*>(prow + ((v ^ (h & 7)) << 4)) =
             make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
       fence_proxy_async_smem();
-      mbar_arrive(&ctl->p_full);
+      mbar_arrive(&ctl->p_full[i & 1]);
     }
     if (ntile > 0) {
-      const bool ok = mbar_wait(&ctl->pv_done, (uint32_t)(ntile - 1) & 1u, abort, p.status);
+      const bool ok =
+          mbar_wait(&ctl->pv_done[(ntile - 1) & 1], (uint32_t)((ntile - 1) >> 1) & 1u, abort, p.status);
       (void)__all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
