@@ -104,7 +104,8 @@ struct Layout {
   static constexpr int rows = qrope + kHeads * kRopeHalf * 2;
   static constexpr int qstage = kQInRing ? stages + (kStages - 2) * kTileBytes : xbuf;
   static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
-  static constexpr int ctl = masks + kMaxRows / 8;
+  static constexpr int rowmax = masks + kMaxRows / 8;     // [2][128] tile row maxima
+  static constexpr int ctl = rowmax + 2 * kHeads * 4;
   static constexpr int total = ctl + 512;
 };
 
@@ -395,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- score exchange: one thread per head row (TMEM lane quadrant warp % 4),
     // running ahead of the softmax.  The partial row goes into the peer's buffer (asynchronous
     // stores that count their bytes on the peer's xfull), the peer's partial is added in the same
-    // order in both CTAs (S_0 + S_1), and the sum goes back into the tile's S columns.
+    // order in both CTAs (S_0 + S_1), and the masked, scaled row z goes back into the tile's S
+    // columns with its maximum in shared memory.
     // Buffer layout [x][chunk c of 4 columns][head] x 16 B: a warp's stores and loads are
     // contiguous.
     const int h = (warp - kXchgWarp0) * 32 + lane;
@@ -428,17 +430,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     peer_xfull + 8u * (uint32_t)x);
       ok = mbar_wait<true>(&ctl->xfull[x], xph, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
+      // z = S * scale * log2(e) for valid slots, -inf for empty ones; and the row maximum
+      float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
+      const uint32_t vm0 = masks_s[2 * i], vm1 = masks_s[2 * i + 1];
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const uint4 o = xbuf[(x * 16 + c) * kHeads + h];
         const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float a = __uint_as_float(sr[4 * c + k]), b2 = __uint_as_float(ov[k]);
-          sr[4 * c + k] = __float_as_uint(half == 0 ? a + b2 : b2 + a);
+          const int col = 4 * c + k;
+          const float a = __uint_as_float(sr[col]), b2 = __uint_as_float(ov[k]);
+          const float sv = half == 0 ? a + b2 : b2 + a;
+          const bool valid = ((col < 32 ? vm0 : vm1) >> (col & 31)) & 1u;
+          const float z = valid ? sv * p.scale_log2 : -INFINITY;
+          sr[col] = __float_as_uint(z);
+          mk[k] = fmaxf(mk[k], z);
         }
       }
+      const float mt = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
       mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);  // our buffer x may be rewritten
+      reinterpret_cast<float*>(smem + Layout::rowmax)[(i & 1) * kHeads + h] = mt;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_st_x16(lane_addr + s_col + (uint32_t)(16 * c), sr + 16 * c);
       tmem_st_wait();
@@ -479,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&ctl->q_tmem);
     }
     for (int i = 0; i < ntile; ++i) {
-      // S = S_0 + S_1 of this tile, summed in TMEM by the exchange warps
+      // z of this tile (S_0 + S_1, masked and scaled) and its row maximum, from the exchange warps
       bool ok = mbar_wait(&ctl->s_sum[i & 1], (uint32_t)(i >> 1) & 1u, abort, p.status);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -487,18 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s_col = kColS + (uint32_t)((i & 1) * kNT);
       tmem_ld_x32(lane_addr + s_col, sr);
       tmem_ld_x32(lane_addr + s_col + 32, sr + 32);
+      const float mt = reinterpret_cast<const float*>(smem + Layout::rowmax)[(i & 1) * kHeads + h];
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&ctl->s_free[i & 1]);
-      float mt = -INFINITY;
-      const uint32_t vm0 = masks_s[2 * i], vm1 = masks_s[2 * i + 1];
-#pragma unroll
-      for (int col = 0; col < kNT; ++col) {
-        const bool valid = ((col < 32 ? vm0 : vm1) >> (col & 31)) & 1u;
-        const float z = valid ? __uint_as_float(sr[col]) * p.scale_log2 : -INFINITY;
-        sr[col] = __float_as_uint(z);
-        mt = fmaxf(mt, z);
-      }
       // lazy rescale: move the reference maximum only when it is exceeded by more than 2^8
       const bool need = mt > m_ref + kRescaleLog2;
       if (__any_sync(0xffffffffu, need && i >= 1 && l_sum > 0.f)) {
@@ -525,18 +529,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (need) m_ref = mt;
       uint32_t pk[32];
-      float ls = 0.f, le = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f}, le[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float p0 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * c]) - m_ref);
         const float p1 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * c + 1]) - m_ref);
         pk[c] = pack_bf16(p0, p1);
         const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&pk[c]);
-        ls += __bfloat162float(r.x) + __bfloat162float(r.y);
-        le += p0 + p1;
+        ls[c & 3] += __bfloat162float(r.x) + __bfloat162float(r.y);
+        le[c & 3] += p0 + p1;
       }
-      l_sum += ls;
-      l_exact += le;
+      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l_exact += (le[0] + le[1]) + (le[2] + le[3]);
       // P row h -> shared memory buffer i & 1, 128-byte swizzled K-major (the A operand of P.V),
       // once the P.V that read it two tiles ago has landed
       if (i >= 2) {
