@@ -561,54 +561,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       (void)__all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
-    // ---------------- epilogue
+    // ---------------- epilogue: the normalised O row goes into the (now idle) ring, 16-byte
+    // chunk c of row h at chunk c ^ (h & 31) so that a warp's stores spread over the banks; all
+    // threads then copy the tile out with coalesced stores after the barrier below
     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
     const float lse2 = l_exact > 0.f ? m_ref + log2f(l_exact) : -INFINITY;
-    if (p.splits == 1) {
-      __nv_bfloat16* orow = p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf;
 #pragma unroll 1
-      for (int c = 0; c < kDvHalf / 32; ++c) {
-        uint32_t o[32];
-        if (ntile > 0) {
-          tmem_ld_x32(lane_addr + kColO + (uint32_t)(c * 32), o);
-          tmem_ld_wait();
-        } else {
+    for (int c = 0; c < kDvHalf / 32; ++c) {
+      uint32_t o[32];
+      if (ntile > 0) {
+        tmem_ld_x32(lane_addr + kColO + (uint32_t)(c * 32), o);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0u;
-        }
-        if (h < p.H) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = w;
-          }
-        }
+        for (int k = 0; k < 32; ++k) o[k] = 0u;
       }
+      if (p.splits == 1) {  // bf16 rows of 512 B: chunks 4c .. 4c+3
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+          *reinterpret_cast<uint4*>(st_s + h * 512 + (((4 * c + v) ^ (h & 31)) << 4)) = w;
+        }
+      } else {  // fp32 rows of 1 KiB: chunks 8c .. 8c+7
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          *reinterpret_cast<float4*>(st_s + h * 1024 + (((8 * c + v) ^ (h & 31)) << 4)) =
+              make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                          __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+      }
+    }
+    if (p.splits == 1) {
       if (half == 0 && h < p.H && p.lse) p.lse[(size_t)t * p.H + h] = lse2 * 0.69314718055994531f;
     } else {
       const size_t unit = ((size_t)t * 2 + half) * p.splits + split;
-      float* po = p.ws_o + (unit * kHeads + h) * kDvHalf;
-#pragma unroll 1
-      for (int c = 0; c < kDvHalf / 32; ++c) {
-        uint32_t o[32];
-        if (ntile > 0) {
-          tmem_ld_x32(lane_addr + kColO + (uint32_t)(c * 32), o);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = 0u;
-        }
-        float4* dst = reinterpret_cast<float4*>(po + c * 32);
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-          __stcg(dst + v, make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                      __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv));
-      }
       __stcg(p.ws_lse + unit * kHeads + h, lse2);
     }
   }
@@ -619,7 +608,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (p.splits == 1) return;
+  // coalesced copy of the staged O tile: a warp writes 512 contiguous bytes
+  if (p.splits == 1) {
+#pragma unroll 4
+    for (int idx = tid; idx < kHeads * 32; idx += kThreads) {
+      const int row = idx >> 5, c = idx & 31;
+      if (row < p.H)
+        *reinterpret_cast<uint4*>(p.out + ((size_t)t * p.H + row) * kDv + half * kDvHalf + c * 8) =
+            *reinterpret_cast<const uint4*>(st_s + row * 512 + ((c ^ (row & 31)) << 4));
+    }
+    return;
+  }
+  {
+    const size_t unit = ((size_t)t * 2 + half) * p.splits + split;
+    float* po = p.ws_o + unit * kHeads * kDvHalf;
+#pragma unroll 4
+    for (int idx = tid; idx < kHeads * 64; idx += kThreads) {
+      const int row = idx >> 6, c = idx & 63;
+      __stcg(reinterpret_cast<float4*>(po + row * kDvHalf + c * 4),
+             *reinterpret_cast<const float4*>(st_s + row * 1024 + ((c ^ (row & 31)) << 4)));
+    }
+  }
+  __threadfence();  // every thread's partial stores are visible before the arrival count
+  __syncthreads();
 
   // ---------------- last CTA of (token, half) merges the split partials
   if (tid == 0) {
@@ -660,6 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float4 acc[kBatch];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
     for (int s = 0; s < p.splits; ++s) {
       float4 x[kBatch];
 #pragma unroll
