@@ -275,6 +275,11 @@ def run_ours(args):
     work = algorithmic(wl, cnt_total)
 
     K = args.steps
+    # Per-kernel events on every SAMPLE-th step only: an event recorded between the two kernels
+    # keeps the attention kernel from starting its prologue during the indexer's tail
+    # (programmatic dependent launch), so the other steps run without one.
+    SAMPLE = 8
+    sampled = [i for i in range(K) if i % SAMPLE == 0]
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     e_all = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     pci = None
@@ -290,18 +295,22 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             e_all[0].record(stream)
             for i in range(K):
-                ev[i][0].record(stream)
-                lib.dsa_li_topk(ctypes.byref(li_args), sp)
-                ev[i][1].record(stream)
-                sfa_entry(ctypes.byref(sfa_args), sp)
-                ev[i][2].record(stream)
+                if i % SAMPLE == 0:
+                    ev[i][0].record(stream)
+                    lib.dsa_li_topk(ctypes.byref(li_args), sp)
+                    ev[i][1].record(stream)
+                    sfa_entry(ctypes.byref(sfa_args), sp)
+                    ev[i][2].record(stream)
+                else:
+                    lib.dsa_li_topk(ctypes.byref(li_args), sp)
+                    sfa_entry(ctypes.byref(sfa_args), sp)
             e_all[1].record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     total_ms = e_all[0].elapsed_time(e_all[1])
-    li_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-    sfa_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    li_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in sampled)
+    sfa_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in sampled)
     if int(status.item()) != 0:
         raise RuntimeError("device status %d in the timed region" % int(status.item()))
     t = torch.tensor([total_ms], device=dev)
@@ -357,7 +366,7 @@ def run_ours(args):
         "config": {**wl.describe(), "l2": "inputs larger than L2: every step streams %.0f MB of key pages "
                    "and gathers from a %.0f MB latent pool" % (work["k_bytes"] / 1e6,
                                                                inp["kv_pool"].numel() * 2 / 1e6),
-                   "launch": "eager C-ABI calls on one stream, CUDA events between kernels"},
+                   "launch": "eager C-ABI calls on one stream; the attention kernel is a programmatic dependent launch; per-kernel CUDA events on every 8th step"},
         "roofline": {"kernel": "li_topk", "bound": "hbm", "achieved": li_achieved, "peak": hbm,
                      "unit": "GB/s", "frac": li_achieved / hbm, "peak_kind": peak_kind,
                      "traffic": traffic, "algorithmic_bytes": work["k_bytes"]},

@@ -467,6 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(ctl->tmem_base, CF::kTmemCols);
   }
 
+  // The next kernel in the stream (sparse attention) may begin its prologue on idle SMs; it reads
+  // nothing this kernel writes before this grid has completed.
+  griddep_launch_dependents();
+
   // ---------------- select phase (cluster-uniform control flow)
   if (tid < T) {
     const int tt = tid;

@@ -43,6 +43,17 @@ DSA_DEV uint32_t elect_one() {
   return pred;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the preceding kernel in the stream has completed and its memory is visible (a no-op
+// when the kernel was launched without programmatic stream serialisation).
+DSA_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the kernel launched after this one with programmatic stream serialisation to begin
+// scheduling its CTAs once every CTA of this grid has passed here (or exited).
+DSA_DEV void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 DSA_DEV void mbar_init(uint64_t* bar, uint32_t count) {

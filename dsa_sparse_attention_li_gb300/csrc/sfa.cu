@@ -186,8 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t = (blockIdx.x >> 1) / p.splits;
   if (t >= p.n_q) return;  // uniform over the pair
   const uint32_t peer = (uint32_t)(half ^ 1);
-  const int b = find_seq(p.q_start, p.B, t);
-  const int L = p.seq_lens[b];
   const int slot0 = split * p.rows_per;
   const int nslot = max(0, min(p.rows_per, p.K - slot0));
 
@@ -220,6 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();  // barriers initialised
   cluster_sync();   // ... in both CTAs of the pair before any remote arrive
+  // The launch may overlap the end of the preceding kernel in the stream (programmatic dependent
+  // launch): everything above touches only this CTA's resources; no global memory is read
+  // before the preceding kernel has completed and its writes are visible.
+  griddep_wait();
+  const int b = find_seq(p.q_start, p.B, t);
+  const int L = p.seq_lens[b];
   if (warp == kMmaWarp && lane == 0 && nslot > 0) {
     // value columns of Q[:, D_r] -> shared memory (moved into TMEM by the softmax warps);
     // issued before the row translation below so the load overlaps it
@@ -873,13 +877,16 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;  // the two value halves of a (token, split)
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // the CTAs may start (barriers, TMEM, cluster handshake) while the preceding kernel finishes
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, sfa_kernel, tm_q, tm_qr, p);
   if (e != cudaSuccess) return cuda_fail(e, "sfa: launch", err);
   return DSA_OK;
