@@ -126,6 +126,11 @@ dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
  * per sequence (one token per CTA pair, no workspace).  Both give the same result up to fp32
  * rounding.
  *
+ * Stream order: both are launched as programmatic dependents of the preceding kernel in the
+ * stream, so their CTAs may start (barrier set-up, tensor-memory allocation) while that kernel
+ * finishes; they read no device memory (inputs included) before it has completed.  Stream order
+ * is therefore kept for every input, whichever kernel wrote it.
+ *
  * Supported: page_size 64; d_qk 576; d_v 512; H in {16, 128} (decode) and 128 (prefill);
  * 1 <= K <= 2048; bf16 q/kv/out.
  */
