@@ -396,6 +396,19 @@ DSA_DEV void st_cluster_v4(uint32_t addr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to the shared memory of a
+// CTA of the cluster (shared::cluster address), counted on that CTA's mbarrier `remote_bar`.
+// The source must have been made visible to the async proxy (fence_proxy_async_smem).
+DSA_DEV void bulk_copy_to_cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                  uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster), "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+DSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk copy of this thread has finished reading its source.
+DSA_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 DSA_DEV uint4 ld_cluster_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"

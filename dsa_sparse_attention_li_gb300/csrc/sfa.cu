@@ -78,6 +78,8 @@ struct Params {
   int B, n_q, H, K, max_pages, num_pages;
   int splits;      // row splits per token
   int rows_per;    // row slots per split (multiple of kNT)
+  int cluster_merge;  // splits == 2: the two splits of a token share a cluster of 4 and merge
+                      // through distributed shared memory (no workspace)
   float scale_log2;  // softmax_scale * log2(e)
   const int* page_table;
   const int* seq_lens;
@@ -120,6 +122,7 @@ struct Ctl {
   int last;  // this CTA merges the splits
   int nvalid;
   int gather_go[2];  // poller's verdict per step (read by all gather threads after bar.sync)
+  uint64_t mrg;      // cluster merge: the other split's rows and lse have arrived
 };
 
 DSA_DEV int find_seq(const int* q_start, int B, int t) {
@@ -185,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = (blockIdx.x >> 1) % p.splits;
   const int t = (blockIdx.x >> 1) / p.splits;
   if (t >= p.n_q) return;  // uniform over the pair
-  const uint32_t peer = (uint32_t)(half ^ 1);
+  const uint32_t crank = cluster_rank();
+  const uint32_t peer = crank ^ 1u;  // the other value half of this (token, split)
   const int slot0 = split * p.rows_per;
   const int nslot = max(0, min(p.rows_per, p.K - slot0));
 
@@ -208,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->xfull[x], 1);  // one local expect_tx arrival + the peer's stored bytes
       mbar_init(&ctl->xfree[x], 128);
     }
+    mbar_init(&ctl->mrg, 1);
     ctl->abort = 0;
     ctl->nvalid = 0;
     fence_barrier_init();
@@ -217,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   __syncthreads();  // barriers initialised
-  cluster_sync();   // ... in both CTAs of the pair before any remote arrive
+  // merge buffers: 64 rows of the other split (64 KiB) and its 64 lse values (256 B)
+  if (p.cluster_merge && tid == 0) mbar_arrive_expect_tx(&ctl->mrg, 64 * 1024 + 64 * 4);
+  cluster_sync();   // ... in every CTA of the cluster before any remote arrive
   // The launch may overlap the end of the preceding kernel in the stream (programmatic dependent
   // launch): everything above touches only this CTA's resources; no global memory is read
   // before the preceding kernel has completed and its writes are visible.
@@ -600,6 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (p.splits == 1) {
       if (half == 0 && h < p.H && p.lse) p.lse[(size_t)t * p.H + h] = lse2 * 0.69314718055994531f;
+    } else if (p.cluster_merge) {
+      reinterpret_cast<float*>(smem + Layout::rowmax)[h] = lse2;  // the tile maxima are done
+      fence_proxy_async_smem();  // the staged rows and lse are read by a bulk copy
     } else {
       const size_t unit = ((size_t)t * 2 + half) * p.splits + split;
       __stcg(p.ws_lse + unit * kHeads + h, lse2);
@@ -621,6 +631,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(p.out + ((size_t)t * p.H + row) * kDv + half * kDvHalf + c * 8) =
             *reinterpret_cast<const uint4*>(st_s + row * 512 + ((c ^ (row & 31)) << 4));
     }
+    return;
+  }
+  if (p.cluster_merge) {
+    // Split s of this half finalises heads [64s, 64s + 64): it sends the other split the staged
+    // rows of that split's heads and their lse, receives its own in the (idle) exchange and P
+    // buffers and the row-maximum area, and combines the two normalised partials by their lse.
+    const int h0 = 64 * split, ph0 = 64 * (split ^ 1);
+    const uint32_t speer = crank ^ 2u;
+    const uint32_t rbar = map_cluster(&ctl->mrg, speer);
+    if (tid == 0) {
+      bulk_copy_to_cluster(map_cluster(smem + Layout::xbuf, speer), st_s + ph0 * 1024, 64 * 1024, rbar);
+      bulk_copy_to_cluster(map_cluster(smem + Layout::rowmax + 128 * 4, speer),
+                           smem + Layout::rowmax + ph0 * 4, 64 * 4, rbar);
+      bulk_commit();
+    }
+    const bool ok = mbar_wait<true>(&ctl->mrg, 0, abort, p.status);
+    const float* lse_own = reinterpret_cast<const float*>(smem + Layout::rowmax);
+    const float* lse_oth = lse_own + 128;  // indexed by head - h0
+    if (ok) {
+#pragma unroll 2
+      for (int item = tid; item < 64 * 64; item += kThreads) {
+        const int hr = item >> 6, c = item & 63, h = h0 + hr;
+        const float lo = lse_own[h], lp = lse_oth[hr];
+        const float M = fmaxf(lo, lp);
+        const float wo = lo == -INFINITY ? 0.f : exp2f(lo - M);
+        const float wp = lp == -INFINITY ? 0.f : exp2f(lp - M);
+        const float W = wo + wp, inv = W > 0.f ? 1.f / W : 0.f;
+        const uint32_t sw = (uint32_t)((c ^ (h & 31)) << 4);
+        const float4 a = *reinterpret_cast<const float4*>(st_s + h * 1024 + sw);
+        const float4 o = *reinterpret_cast<const float4*>(smem + Layout::xbuf + hr * 1024 + sw);
+        // split 0's term first in both CTAs
+        const float4 x0 = split == 0 ? a : o, x1 = split == 0 ? o : a;
+        const float w0 = (split == 0 ? wo : wp) * inv, w1 = (split == 0 ? wp : wo) * inv;
+        if (h < p.H) {
+          uint2 v;
+          v.x = pack_bf16(w0 * x0.x + w1 * x1.x, w0 * x0.y + w1 * x1.y);
+          v.y = pack_bf16(w0 * x0.z + w1 * x1.z, w0 * x0.w + w1 * x1.w);
+          *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf + c * 4) = v;
+        }
+      }
+      if (half == 0 && tid < 64 && h0 + tid < p.H && p.lse) {
+        const float lo = lse_own[h0 + tid], lp = lse_oth[tid];
+        const float M = fmaxf(lo, lp);
+        const float W = (lo == -INFINITY ? 0.f : exp2f(lo - M)) + (lp == -INFINITY ? 0.f : exp2f(lp - M));
+        p.lse[(size_t)t * p.H + h0 + tid] = W > 0.f ? (M + log2f(W)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    if (tid == 0) bulk_wait_read_all();  // the outgoing copy has read its source
     return;
   }
   {
@@ -762,6 +820,7 @@ __global__ void __launch_bounds__(128) sfa_cuda_core_kernel(const Params p) {
 
 struct Plan {
   int splits, rows_per;
+  bool cluster_merge;  // two splits merged through distributed shared memory (cluster of 4)
 };
 
 static Plan plan(const dsa_sfa_args& a, bool prefill, int sm_count) {
@@ -785,11 +844,12 @@ static Plan plan(const dsa_sfa_args& a, bool prefill, int sm_count) {
   splits = (a.K + rows_per - 1) / rows_per;
   pl.splits = splits;
   pl.rows_per = rows_per;
+  pl.cluster_merge = splits == 2;
   return pl;
 }
 
 static size_t ws_bytes(const dsa_sfa_args& a, const Plan& pl) {
-  if (pl.splits <= 1) return 0;
+  if (pl.splits <= 1 || pl.cluster_merge) return 0;
   const size_t units = (size_t)a.n_q * 2 * pl.splits;
   size_t bytes = units * kHeads * kDvHalf * 4;   // partial o
   bytes += units * kHeads * 4;                    // partial lse
@@ -827,6 +887,7 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   p.num_pages = a.num_pages;
   p.splits = pl.splits;
   p.rows_per = pl.rows_per;
+  p.cluster_merge = pl.cluster_merge ? 1 : 0;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   p.page_table = a.page_table;
   p.seq_lens = a.seq_lens;
@@ -870,8 +931,9 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   if (e != cudaSuccess) return cuda_fail(e, "sfa: set shared memory size", err);
   const unsigned grid = (unsigned)(a.n_q * 2 * pl.splits);
   if (std::getenv("DSA_VERBOSE"))
-    std::fprintf(stderr, "[dsa] sfa %s splits=%d rows_per=%d grid=%u smem=%d\n",
-                 prefill ? "prefill" : "decode", pl.splits, pl.rows_per, grid, smem);
+    std::fprintf(stderr, "[dsa] sfa %s splits=%d rows_per=%d cluster_merge=%d grid=%u smem=%d\n",
+                 prefill ? "prefill" : "decode", pl.splits, pl.rows_per, (int)pl.cluster_merge, grid,
+                 smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -879,7 +941,8 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;  // the two value halves of a (token, split)
+  // the two value halves of a (token, split); with a cluster merge both splits of a token
+  attr[0].val.clusterDim.x = pl.cluster_merge ? 4 : 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   // the CTAs may start (barriers, TMEM, cluster handshake) while the preceding kernel finishes

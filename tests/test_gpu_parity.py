@@ -79,6 +79,20 @@ def test_prefill_small(cuda_lib):
     check_sfa(inp_cpu, g, toks)
 
 
+@pytest.mark.parametrize("splits", ["1", "2", "3"])
+def test_decode_row_split_counts(cuda_lib, splits, monkeypatch):
+    """One split (no merge), two (the splits of a token merge through distributed shared memory
+    in a cluster of four) and three (partials merged through the workspace) give the oracle's
+    attention on the same index sets."""
+    monkeypatch.setenv("DSA_SFA_SPLITS", splits)
+    inp_cpu, inp = _small("decode_32k", seq_lens=[5000, 3000, 129], n_new=[1, 2, 1])
+    g = run_gpu(inp, prefill=False)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    check_indices(inp_cpu, g, toks, exact=False)
+    check_sfa(inp_cpu, g, toks)
+
+
 def test_decode_and_prefill_attention_agree(cuda_lib):
     inp_cpu, inp = _small("decode_32k", seq_lens=[4000, 5000], n_new=[1, 1])
     a = run_gpu(inp, prefill=False)
