@@ -145,6 +145,25 @@ DSA_DEV uint32_t block_excl_suffix(uint32_t v, uint32_t* scratch) {
   return above + x - v;
 }
 
+// Adds the 8 packed 16-bit bins of histogram words h[0..3] of every CTA of the cluster (C CTAs)
+// into cnt; the DSMEM loads of up to four CTAs are in flight together.
+DSA_DEV void cluster_hist_sum(const uint32_t* h, int C, uint32_t* cnt) {
+#pragma unroll 1
+  for (int r0 = 0; r0 < C; r0 += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = r0 + u < C ? ld_cluster_v4(map_cluster(h, (uint32_t)(r0 + u))) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      cnt[0] += v[u].x & 0xffffu; cnt[1] += v[u].x >> 16;
+      cnt[2] += v[u].y & 0xffffu; cnt[3] += v[u].y >> 16;
+      cnt[4] += v[u].z & 0xffffu; cnt[5] += v[u].z >> 16;
+      cnt[6] += v[u].w & 0xffffu; cnt[7] += v[u].w >> 16;
+    }
+  }
+}
+
 // Inclusive sum over the lanes of the warp.
 DSA_DEV uint32_t warp_incl_scan(uint32_t v) {
   const int lane = threadIdx.x & 31;
@@ -500,13 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       if (tid < kHistThreads) {
         const uint32_t* h = hist + tt * kHistWords + 4 * tid;
-        for (int r = 0; r < p.C; ++r) {
-          const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
-          cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
-          cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
-          cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
-          cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
-        }
+        cluster_hist_sum(h, p.C, cnt);
       }
       uint32_t sum = 0;
 #pragma unroll
@@ -816,13 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
           if (tid < kHistThreads) {
             const uint32_t* h = hb + tt * kHistWords + 4 * tid;
-            for (int r = 0; r < p.C; ++r) {
-              const uint4 v = ld_cluster_v4(map_cluster(h, (uint32_t)r));
-              cnt[0] += v.x & 0xffffu; cnt[1] += v.x >> 16;
-              cnt[2] += v.y & 0xffffu; cnt[3] += v.y >> 16;
-              cnt[4] += v.z & 0xffffu; cnt[5] += v.z >> 16;
-              cnt[6] += v.w & 0xffffu; cnt[7] += v.w >> 16;
-            }
+            cluster_hist_sum(h, p.C, cnt);
           }
           uint32_t sum = 0;
 #pragma unroll
