@@ -117,6 +117,7 @@ struct Ctl {
   int wgt[4][kThreads / 32], weq[4][kThreads / 32];  // per-warp counts above / at the threshold
   // candidate path of the select (see the select phase)
   int cand_total[4];          // keys of the whole cluster in the threshold bin of the first pass
+  int few_cnt;                // candidates sharing the 22-bit prefix (local resolution)
   int own_cnt[4];             // this CTA's candidates (read by the cluster)
   int rn[4][kMaxCluster], roff[4][kMaxCluster];    // candidates per rank and their offsets
   int rsure[4][kMaxCluster];  // per rank: keys certainly selected (above the first-pass bin)
@@ -550,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Candidate path when every threshold bin is small enough to gather into one CTA.
     const int cap = p.nstage * CF::kTileBytes / 2 / 8 / T;
-    fast = true;
+    // a lane's candidate bits (4 per 128-key step of its warp segment) fit one 64-bit word
+    fast = p.chunk <= 16 * 128 * (kThreads / 32);
 #pragma unroll
     for (int tt = 0; tt < T; ++tt)
       if (ctl->radix[tt] && ctl->cand_total[tt] > cap) fast = false;  // uniform over the cluster
@@ -565,69 +567,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cap = p.nstage * CF::kTileBytes / 2 / 8 / T;
     uint2* own_list = reinterpret_cast<uint2*>(stage_base);
     uint2* gath = reinterpret_cast<uint2*>(stage_base + p.nstage * CF::kTileBytes / 2);
-    // a1: count per warp segment
-#pragma unroll 1
+    // a1: one pass over the warp's segment: sure keys counted, candidates marked (bit 4*step + k
+    // of the lane's word) and counted per lane; then a warp scan of the lane counts
+    uint64_t cbits[4];
+    int lane_base[4];
+#pragma unroll
+    for (int tt = 0; tt < 4; ++tt) {
+      cbits[tt] = 0ull;
+      lane_base[tt] = 0;
+    }
+#pragma unroll
     for (int tt = 0; tt < T; ++tt) {
       const bool rdx = ctl->radix[tt] != 0;
       const uint32_t b0 = ctl->prefix[tt] >> 21;
       const uint32_t* sc = scores + tt * p.chunk;
-      uint32_t sure = 0, cand = 0;
-#pragma unroll 4
-      for (int e = e_lo + 4 * lane; e < e_hi; e += 128) {
+      uint32_t sure = 0;
+      uint64_t bits = 0ull;
+#pragma unroll 2
+      for (int e = e_lo + 4 * lane, it = 0; e < e_hi; e += 128, ++it) {
         const uint4 v = *reinterpret_cast<const uint4*>(sc + e);
         const uint32_t us[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           sure += rdx ? ((us[k] >> 21) > b0) : (us[k] != 0u);
-          cand += (rdx && us[k] != 0u && (us[k] >> 21) == b0);
+          if (rdx && us[k] != 0u && (us[k] >> 21) == b0) bits |= 1ull << (4 * it + k);
         }
       }
+      const uint32_t mine = (uint32_t)__popcll(bits);
+      const uint32_t inc = warp_incl_scan(mine);
+      cbits[tt] = bits;
+      lane_base[tt] = (int)(inc - mine);
       sure = __reduce_add_sync(0xffffffffu, sure);
-      cand = __reduce_add_sync(0xffffffffu, cand);
+      const uint32_t cand = __shfl_sync(0xffffffffu, inc, 31);
       if (lane == 0) {
         ctl->wgt[tt][warp] = (int)sure;
         ctl->weq[tt][warp] = (int)cand;  // candidates of the warp (replaced in step d)
       }
     }
     __syncthreads();
-    // a2: write the candidates in ascending position order (warp segments are in order)
-#pragma unroll 1
+    // a2: each lane writes its candidates (lane-major within the warp; a warp's candidates stay
+    // contiguous and in warp order, which is all the per-warp counting below needs)
+#pragma unroll
     for (int tt = 0; tt < T; ++tt) {
       if (!ctl->radix[tt]) continue;
-      const uint32_t b0 = ctl->prefix[tt] >> 21;
       const uint32_t* sc = scores + tt * p.chunk;
-      int run = 0;
-      for (int w = 0; w < warp; ++w) run += ctl->weq[tt][w];
+      int slot = lane_base[tt];
+      for (int w = 0; w < warp; ++w) slot += ctl->weq[tt][w];
       uint2* dst = own_list + tt * cap;
-      // batches of four 128-key groups: lane holds keys 4*lane..4*lane+3 of each group
-#pragma unroll 1
-      for (int eb = e_lo; eb < e_hi; eb += 512) {
-        uint32_t key[16];
-        uint32_t fc = 0;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (eb + 128 * g < e_hi) v = *reinterpret_cast<const uint4*>(sc + eb + 128 * g + 4 * lane);
-          key[4 * g + 0] = v.x; key[4 * g + 1] = v.y; key[4 * g + 2] = v.z; key[4 * g + 3] = v.w;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (key[4 * g + k] != 0u && (key[4 * g + k] >> 21) == b0) fc |= 1u << (4 * g + k);
-        }
-        const uint32_t cnt = nibble_counts(fc);
-        const uint32_t inc = warp_incl_scan(cnt);
-        const uint32_t tot = __shfl_sync(0xffffffffu, inc, 31);
-        const uint32_t exc = inc - cnt;
-        int base = run;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          int slot = base + (int)((exc >> (8 * g)) & 0xffu);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if ((fc >> (4 * g + k)) & 1u)
-              dst[slot++] = make_uint2(key[4 * g + k], (uint32_t)(lo + eb + 128 * g + 4 * lane + k));
-          base += (int)((tot >> (8 * g)) & 0xffu);
-        }
-        run = base;
+      uint64_t bits = cbits[tt];
+      while (bits) {
+        const int bit = __ffsll((long long)bits) - 1;
+        bits &= bits - 1ull;
+        const int e = e_lo + 128 * (bit >> 2) + 4 * lane + (bit & 3);
+        dst[slot++] = make_uint2(sc[e], (uint32_t)(lo + e));
       }
     }
     __syncthreads();
@@ -683,32 +675,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     cluster_arrive();  // this CTA has finished reading the other CTAs' shared memory
     __syncthreads();
-    // (c) the remaining 21 bits among the gathered candidates, locally (no cluster barrier)
+    // (c) the remaining 21 bits among the gathered candidates, locally (no cluster barrier):
+    // a histogram of bits 20..10, then the last 10 bits directly among the few candidates that
+    // share the 22-bit prefix (a histogram again when there are more than kFew)
+    constexpr int kFew = 64;
+    uint32_t* few = hist + kHistWords;  // scratch beside the local histogram
 #pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
       if (!ctl->radix[tt]) continue;
       const int n = ctl->cand_total[tt];
       const uint2* G = gath + tt * cap;
-      uint32_t* h = hist + tt * kHistWords;
-#pragma unroll 1
-      for (int pass = 1; pass < 3; ++pass) {
-        const int shift = pass == 1 ? 10 : 0;
-        const uint32_t bmask = pass == 1 ? 2047u : 1023u;
+      uint32_t* h = hist;
+      {  // bits 20..10
         const uint32_t pref = ctl->prefix[tt];
-        const uint32_t pmask = pass == 1 ? 0xffe00000u : 0xfffffc00u;
         for (int i = tid; i < kHistWords; i += kThreads) h[i] = 0u;
+        if (tid == 0) ctl->few_cnt = 0;
         __syncthreads();
         for (int i = tid; i < n; i += kThreads) {
           const uint32_t u = G[i].x;
-          if ((u & pmask) == pref) {
-            const uint32_t bin = (u >> shift) & bmask;
+          if ((u & 0xffe00000u) == pref) {
+            const uint32_t bin = (u >> 10) & 2047u;
             atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
           }
         }
         __syncthreads();
         find_bin_local(h, (uint32_t)ctl->need[tt], tt, ctl);
         if (tid == 0) {
-          ctl->prefix[tt] |= (uint32_t)ctl->found_bin[tt] << shift;
+          ctl->prefix[tt] |= (uint32_t)ctl->found_bin[tt] << 10;
+          ctl->need[tt] = ctl->found_need[tt];
+        }
+        __syncthreads();
+      }
+      const uint32_t pref = ctl->prefix[tt];
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t u = G[i].x;
+        if ((u & 0xfffffc00u) == pref) {
+          const int slot = atomicAdd(&ctl->few_cnt, 1);
+          if (slot < kFew) few[slot] = u;
+        }
+      }
+      __syncthreads();
+      const int m = ctl->few_cnt;  // uniform over the block
+      if (m <= kFew) {
+        // the need-th largest of the m keys: the key with (greater) < need <= (greater or equal)
+        if (tid < m) {
+          const uint32_t v = few[tid];
+          int gt = 0, ge = 0;
+          for (int j = 0; j < m; ++j) {
+            gt += few[j] > v;
+            ge += few[j] >= v;
+          }
+          const int need = ctl->need[tt];
+          if (gt < need && need <= ge) {  // equal keys write equal values
+            ctl->found_bin[tt] = (int)v;
+            ctl->found_need[tt] = need - gt;
+          }
+        }
+        __syncthreads();
+        if (tid == 0) {
+          ctl->prefix[tt] = (uint32_t)ctl->found_bin[tt];
+          ctl->need[tt] = ctl->found_need[tt];
+        }
+        __syncthreads();
+      } else {  // bits 9..0 by histogram
+        for (int i = tid; i < kHistWords; i += kThreads) h[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t u = G[i].x;
+          if ((u & 0xfffffc00u) == pref) {
+            const uint32_t bin = u & 1023u;
+            atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
+          }
+        }
+        __syncthreads();
+        find_bin_local(h, (uint32_t)ctl->need[tt], tt, ctl);
+        if (tid == 0) {
+          ctl->prefix[tt] |= (uint32_t)ctl->found_bin[tt];
           ctl->need[tt] = ctl->found_need[tt];
         }
         __syncthreads();
