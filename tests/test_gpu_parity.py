@@ -79,6 +79,20 @@ def test_prefill_small(cuda_lib):
     check_sfa(inp_cpu, g, toks)
 
 
+@pytest.mark.parametrize("splits", ["2", "4"])
+def test_integer_config_row_splits_16_heads(cuda_lib, splits, monkeypatch):
+    """16 SFA heads (padded to 128 on chip) through the on-chip merge of two splits and the
+    workspace merge of four, on the integer-exact indexer config."""
+    monkeypatch.setenv("DSA_SFA_SPLITS", splits)
+    inp_cpu, inp = _small("decode_int_4k", seq_lens=[4096, 700], n_new=[1, 2])
+    g = run_gpu(inp, prefill=False)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    n_exact, _ = check_indices(inp_cpu, g, toks, exact=True)
+    assert n_exact == len(toks)
+    check_sfa(inp_cpu, g, toks)
+
+
 @pytest.mark.parametrize("splits", ["1", "2", "3"])
 def test_decode_row_split_counts(cuda_lib, splits, monkeypatch):
     """One split (no merge), two (the splits of a token merge through distributed shared memory
