@@ -14,16 +14,19 @@
 //   streaming phase  warp 0 issues TMA loads of two 64-row key pages per 128-key tile (page ids
 //                    resolved through the page table), warp 1 issues tcgen05.mma
 //                    D[128 keys x T*H_I] = K_tile . Q^T into a double-buffered TMEM accumulator,
-//                    warps 4..7 (one TMEM lane = one key per thread) apply ReLU, the head weights
-//                    and the head sum, mask by causality and length, and store an order-preserving
-//                    32-bit key of each score in shared memory;
-//   select phase     three radix passes (11/11/10 bits; the first histogram is built by the
-//                    epilogue while keys stream) give per-CTA histograms whose cluster total is
-//                    read over distributed shared memory; every CTA derives the same K-th key
-//                    and the number of ties to take; per-warp counts give each warp its output
-//                    offset and tie quota (ties go to the lowest positions; CTAs and warps own
-//                    ascending position ranges), and a warp-ballot compaction writes the
-//                    positions in ascending order.
+//                    warps 4..7 and 8..11 (one per accumulator buffer; one TMEM lane = one key per
+//                    thread) apply ReLU, the head weights and the head sum, mask by causality and
+//                    length, store an order-preserving 32-bit key of each score in shared memory
+//                    and build the histogram of its top 11 bits;
+//   select phase     every CTA reads the cluster's histograms over distributed shared memory and
+//                    finds the bin of the K-th key.  Usually the cluster's keys in that bin are few
+//                    enough to gather: each CTA lists its own, one cluster barrier publishes the
+//                    lists, and every CTA resolves the remaining 21 bits locally.  Otherwise two
+//                    more cluster-wide radix passes (11 and 10 bits) follow.  Every CTA derives
+//                    the same K-th key and the number of ties to take; per-warp counts give each
+//                    warp its output offset and tie quota (ties go to the lowest positions; CTAs
+//                    and warps own ascending position ranges), and a packed warp-scan compaction
+//                    writes the positions in ascending order.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>

@@ -11,27 +11,31 @@
 // blocks); "Day0 Inference Adaptation ... CANN", section 3.1 (SFA reads the main attention KV at
 // the indexer's positions).
 //
-// Work decomposition.  A cluster of two CTAs (16 warps each) serves one (query token t, row
-// split s); CTA r of the pair owns the value columns [256r, 256r + 256) and, for Q.K^T, the
-// head dimensions D_r = [256r, 256r + 256) + [512 + 32r, 512 + 32r + 32) (half of the 576):
-//   - Q[t] restricted to D_r (128 heads x 288, bf16) lives in TMEM as the A operand of all 18
-//     k-steps of the partial product S_r = Q[:, D_r].K[:, D_r]^T;
+// Work decomposition.  A pair of CTAs (16 warps each) serves one (query token t, row split s);
+// CTA r of the pair owns the value columns [256r, 256r + 256) and, for Q.K^T, the head
+// dimensions D_r = [256r, 256r + 256) + [512 + 32r, 512 + 32r + 32) (half of the 576):
+//   - Q[t] on D_r: the 256 value dimensions live in TMEM (A operand of 16 k-steps), the 32 rope
+//     dimensions in shared memory (64-byte swizzle, A operand of 2 k-steps);
 //   - the split's selected positions are translated to physical rows (page table) in shared
-//     memory; eight gather warps copy, per 64-row tile, only the 640 bytes of each row the CTA
-//     uses (its 512 value bytes and the 128 rope bytes) with 16-byte cp.async (empty slots are
-//     zero-filled) into a 3-stage ring laid out [box][row][128 B] with the 128-byte swizzle, so a
-//     stage is the K-major B operand of Q.K^T (N = 64 rows) and the MN-major B operand of P.V
-//     (K = 64 rows, N = 256);
-//   - the two CTAs exchange their partial S tiles through distributed shared memory (fp32,
-//     mbarrier-signalled), so both hold the same S = S_0 + S_1; one thread per head (TMEM lane)
-//     masks, scales and exponentiates its row, writes P (bf16) back to TMEM and accumulates the
-//     row sum in fp32; the reference maximum only moves when a tile's maximum exceeds it by more
-//     than 2^8, and only then is the head's O row rescaled in TMEM;
+//     memory; seven gather warps copy, per 64-row tile, only the 576 bytes of each row the CTA
+//     uses (its 512 value bytes and 64 rope bytes) with 16-byte cp.async (empty slots are
+//     zero-filled) into a 4-stage ring (value boxes [box][row][128 B] with the 128-byte swizzle,
+//     rope box with 64-byte rows), so a stage is the K-major B operand of Q.K^T (N = 64 rows)
+//     and its value boxes the MN-major B operand of P.V (K = 64 rows, N = 256);
+//   - S_r = Q[:, D_r].K[:, D_r]^T goes to one of two TMEM buffers; four exchange warps send S_r
+//     to the peer through distributed shared memory (asynchronous stores counted on the peer's
+//     mbarrier), add the peer's partial in the same order in both CTAs (S_0 + S_1), mask and
+//     scale it and take the row maximum, one tile ahead of the softmax;
+//   - one softmax thread per head (TMEM lane) exponentiates its row, writes P (bf16) into one of
+//     two shared-memory buffers (A operand of P.V) and accumulates the row sums in fp32; the
+//     reference maximum only moves when a tile's maximum exceeds it by more than 2^8, and only
+//     then is the head's O row rescaled in TMEM;
 //   - O (128 x 256 fp32 = half of TMEM) accumulates P.V_r across tiles.
 // Each head's 128x512 fp32 O would fill all of TMEM, hence the value split over the pair; the
 // split of the Q.K^T dimensions halves both the gathered bytes and the tensor work of each CTA.
-// With several row splits the partial (o, lse) are written to the caller's workspace and the
-// last CTA of a (token, r) to finish merges them.
+// With two row splits both pairs of a token form one cluster of four and merge their normalised
+// partials through distributed shared memory; with more, the partial (o, lse) go to the
+// caller's workspace and the last CTA of a (token, r) to finish merges them.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
