@@ -116,6 +116,18 @@ def test_decode_and_prefill_attention_agree(cuda_lib):
     assert d <= 2e-2, d
 
 
+@pytest.mark.parametrize("prefill", [False, True])
+def test_sequence_without_new_tokens(cuda_lib, prefill):
+    """A sequence of the batch with no query tokens (equal consecutive q_start) contributes no
+    rows and does not disturb its neighbours."""
+    inp_cpu, inp = _small("decode_32k", seq_lens=[3000, 2000, 4000], n_new=[1, 0, 2])
+    g = run_gpu(inp, prefill=prefill)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    check_indices(inp_cpu, g, toks, exact=False)
+    check_sfa(inp_cpu, g, toks)
+
+
 def test_k_covers_context_selects_everything(cuda_lib):
     inp_cpu, inp = _small("decode_32k", seq_lens=[1500, 64, 2048], n_new=[1, 2, 1])
     g = run_gpu(inp)
