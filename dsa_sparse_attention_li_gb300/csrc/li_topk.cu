@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Cluster-uniform validity (every CTA of the cluster reads the same values).
   if (g == p.groups - 1 && rank == 0 && tid == 0 && n_b > p.groups * T)
     report(p.status, kStatusDeviceCheck);
-  if (n_b < 0 || L < n_b || L > p.C * p.chunk || qs < 0 || qs + n_b > p.n_q) {
+  if (n_b < 0 || L < n_b || L > p.C * p.chunk || L > p.max_pages * 64 || qs < 0 ||
+      qs + n_b > p.n_q) {
     if (rank == 0 && tid == 0) report(p.status, kStatusDeviceCheck);
     return;
   }

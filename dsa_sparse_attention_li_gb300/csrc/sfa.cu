@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // before the preceding kernel has completed and its writes are visible.
   griddep_wait();
   const int b = find_seq(p.q_start, p.B, t);
-  const int L = p.seq_lens[b];
+  const int L = min(p.seq_lens[b], p.max_pages * 64);  // positions the page table covers
   if (warp == kMmaWarp && lane == 0 && nslot > 0) {
     // value columns of Q[:, D_r] -> shared memory (moved into TMEM by the softmax warps);
     // issued before the row translation below so the load overlaps it
@@ -774,7 +774,7 @@ __global__ void __launch_bounds__(128) sfa_cuda_core_kernel(const Params p) {
   __shared__ float red[4];
   const int t = blockIdx.x / p.H, h = blockIdx.x % p.H, tid = threadIdx.x;
   const int b = find_seq(p.q_start, p.B, t);
-  const int L = p.seq_lens[b];
+  const int L = min(p.seq_lens[b], p.max_pages * 64);  // positions the page table covers
   const __nv_bfloat16* qh = p.q + ((size_t)t * p.H + h) * kDqk;
   float m = -INFINITY;
   for (int r = tid; r < p.K; r += 128) {

@@ -160,6 +160,26 @@ def test_bad_page_id_sets_status_without_fault(cuda_lib):
     torch.cuda.synchronize()  # the context is still usable
 
 
+def test_sequence_longer_than_page_table_sets_status_without_fault(cuda_lib):
+    """A sequence length past what the page table covers is reported, never read past."""
+    inp_cpu, inp = _small("decode_32k", seq_lens=[3000], n_new=[1])
+    wl = inp["wl"]
+    pt_k, pt_kv = inp["pt_k"][:, :20].contiguous(), inp["pt_kv"][:, :20].contiguous()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.full((wl.n_q, wl.K), -1, dtype=torch.int32, device="cuda")
+    dsa.li_topk(inp["q_li"], inp["w"], inp["k_pool"], pt_k, inp["seq_lens"], inp["q_start"], wl.K,
+                max_seq_len=20 * 64, max_q_per_seq=1, out_idx=idx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == dsa.DSA_ERR_DEVICE_CHECK
+    status.zero_()
+    idx[:, :8] = torch.arange(1272, 1280 + 7 * 8, 8, dtype=torch.int32)  # last 7 past coverage
+    dsa.sfa_decode(inp["q_sfa"], inp["kv_pool"], pt_kv, inp["seq_lens"], inp["q_start"], idx,
+                   softmax_scale=wl.softmax_scale, max_seq_len=20 * 64, max_q_per_seq=1,
+                   status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == dsa.DSA_ERR_DEVICE_CHECK
+
+
 def test_cache_write_roundtrip(cuda_lib):
     inp_cpu, inp = _small("decode_32k", seq_lens=[200, 100], n_new=[1, 1])
     pool = torch.zeros_like(inp["kv_pool"])
