@@ -7,11 +7,13 @@ the same bytes it produces are consumed by the CPU oracle (``oracle/``) and by t
 
 Layouts (all row-major, C order):
 
-* ``q_li``     [n_q, H_I, d_I]  bf16, or float8_e4m3fn for the quantised indexer path
+* ``q_li``     [n_q, H_I, d_I]  bf16, or float8_e4m3fn for the quantised indexer paths
 * ``q_scale``  [n_q, H_I]       fp32 (fp8 only; one scale per query token, replicated over heads)
+* ``q_sf``     [n_q, H_I, d_I/32] uint8 E8M0 block scales (mxfp8 only: one per 32 elements)
 * ``w``        [n_q, H_I]       fp32 index-head weights
 * ``k_pool``   [pages_k, 64, d_I]  paged index-key cache (bf16 or e4m3)
 * ``k_scale``  [pages_k, 64]    fp32 per-row key scale (fp8 only)
+* ``k_sf``     [pages_k, 64, d_I/32] uint8 E8M0 block scales of the key rows (mxfp8 only)
 * ``pt_k``     [B, max_pages]   int32 page table of the key cache
 * ``q_sfa``    [n_q, H, 576]    bf16 attention queries (512 latent + 64 rope)
 * ``kv_pool``  [pages_kv, 64, 576] bf16 paged MLA latent cache; the value is its first 512 columns
@@ -47,7 +49,7 @@ class Workload:
     d_I: int
     K: int
     H: int
-    li_dtype: str = "bf16"          # "bf16" | "fp8"
+    li_dtype: str = "bf16"          # "bf16" | "fp8" | "mxfp8"
     values: str = "normal"          # "normal" (N(0,1)) | "int4" (integers uniform in [-4, 4])
     w_values: str = "normal"        # "normal" (N(0,1)/sqrt(H_I)) | "int14" (integers in [1, 4])
     seed: int = 0
@@ -99,6 +101,7 @@ def preset(name: str) -> Workload:
                       integer-valued bf16 inputs (scores exact in fp32)
     decode_32k      : 32 sequences x 1 token, L=32768, 64x128 index heads, K=2048, 128 heads
     decode_32k_fp8  : decode_32k with e4m3 index q/k and per-token fp32 scales
+    decode_32k_mxfp8: decode_32k with MXFP8 index q/k (e4m3 elements, one E8M0 scale per 32)
     specdec_ragged  : 64 sequences x 2 tokens (verified + draft), L log-uniform in [1024, 131072]
     prefill_64k     : 1 sequence, 4096 new tokens appended to a 61440-token prefix
     """
@@ -110,6 +113,9 @@ def preset(name: str) -> Workload:
     if name == "decode_32k_fp8":
         return Workload(name, [32768] * 32, [1] * 32, H_I=64, d_I=128, K=2048, H=128,
                         li_dtype="fp8", seed=1003)
+    if name == "decode_32k_mxfp8":
+        return Workload(name, [32768] * 32, [1] * 32, H_I=64, d_I=128, K=2048, H=128,
+                        li_dtype="mxfp8", seed=1006)
     if name == "specdec_ragged":
         lens = _log_uniform_lengths(64, 1024, 131072, seed=1004)
         return Workload(name, lens, [2] * 64, H_I=64, d_I=128, K=2048, H=128, seed=1004)
@@ -118,7 +124,8 @@ def preset(name: str) -> Workload:
     raise KeyError(name)
 
 
-PRESETS = ["decode_int_4k", "decode_32k", "decode_32k_fp8", "specdec_ragged", "prefill_64k"]
+PRESETS = ["decode_int_4k", "decode_32k", "decode_32k_fp8", "decode_32k_mxfp8", "specdec_ragged",
+           "prefill_64k"]
 
 
 def small(name: str, **over) -> Workload:
@@ -145,6 +152,31 @@ def _quant_e4m3(x: torch.Tensor, dim: int):
     scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
     q = (x / scale).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
     return q, scale.squeeze(dim).to(torch.float32)
+
+
+MX_GROUP = 32
+E4M3_EMAX = 8  # exponent of the largest normal e4m3 value (448 = 1.75 * 2^8)
+
+
+def _quant_mx(x: torch.Tensor):
+    """MX quantisation of the last dimension in groups of 32 (OCP Microscaling Formats v1.0):
+    shared scale X = 2^(floor(log2(amax)) - 8) stored as an E8M0 byte (exponent + 127; 127 when
+    amax == 0), elements x / X rounded to nearest-even e4m3 and clamped to +-448."""
+    shape = x.shape
+    g = x.reshape(*shape[:-1], shape[-1] // MX_GROUP, MX_GROUP)
+    amax = g.abs().amax(dim=-1, keepdim=True)
+    _, e = torch.frexp(amax)                     # amax = m * 2^e, m in [0.5, 1)
+    shared = torch.where(amax > 0, e - 1 - E4M3_EMAX, torch.zeros_like(e)).clamp(-127, 127)
+    q = (g / torch.ldexp(torch.ones_like(amax), shared)).clamp(-FP8_MAX, FP8_MAX)
+    q = q.to(torch.float8_e4m3fn).reshape(shape)
+    return q, (shared.squeeze(-1) + 127).to(torch.uint8)
+
+
+def _int_mx(x: torch.Tensor, g: torch.Generator):
+    """Integer-valued elements (exact in e4m3) with E8M0 scales drawn from {2^-1, 2^0, 2^1}."""
+    sf = torch.randint(126, 129, (*x.shape[:-1], x.shape[-1] // MX_GROUP), generator=g,
+                       device=x.device).to(torch.uint8)
+    return x.to(torch.float8_e4m3fn), sf
 
 
 def _page_table(pages: List[int], max_pages: int, g: torch.Generator) -> torch.Tensor:
@@ -203,7 +235,16 @@ def generate(wl: Workload, device="cpu") -> dict:
         w = torch.randint(1, 5, (n_q, wl.H_I), generator=gv, device=device).to(torch.float32)
     else:
         w = torch.randn((n_q, wl.H_I), generator=gv, device=device) / math.sqrt(wl.H_I)
-    if wl.li_dtype == "fp8":
+    if wl.li_dtype == "mxfp8":
+        gm = torch.Generator(device=device).manual_seed(wl.seed + 104729)
+        quant = (lambda x: _int_mx(x, gm)) if wl.values == "int4" else _quant_mx
+        q8, qsf = quant(q)
+        k8, ksf = quant(k)
+        out["q_li"], out["q_sf"] = q8.contiguous(), qsf.contiguous()
+        out["k_pool"], out["k_sf"] = k8.contiguous(), ksf.contiguous()
+        out["q_scale"] = None
+        out["k_scale"] = None
+    elif wl.li_dtype == "fp8":
         q8, qs = _quant_e4m3(q.reshape(n_q, -1), dim=1)
         out["q_li"] = q8.view(n_q, wl.H_I, wl.d_I)
         out["q_scale"] = qs[:, None].expand(n_q, wl.H_I).contiguous()
@@ -250,7 +291,7 @@ def repage(inp: dict, seed: int) -> dict:
     wl = inp["wl"]
     g = torch.Generator().manual_seed(seed)
     out = dict(inp)
-    for pool_key, pt_key, sc_key in (("k_pool", "pt_k", "k_scale"), ("kv_pool", "pt_kv", None)):
+    for pool_key, pt_key, sc_keys in (("k_pool", "pt_k", ("k_scale", "k_sf")), ("kv_pool", "pt_kv", ())):
         old_pt = inp[pt_key].cpu()
         new_pt = _page_table(wl.pages(), wl.max_pages, g)
         pool = inp[pool_key]
@@ -261,7 +302,9 @@ def repage(inp: dict, seed: int) -> dict:
         dst_t = torch.tensor(dst, device=pool.device)
         new_pool.view(pool.shape[0], -1)[dst_t] = pool.view(pool.shape[0], -1)[src_t]
         out[pool_key] = new_pool
-        if sc_key and inp.get(sc_key) is not None:
+        for sc_key in sc_keys:
+            if inp.get(sc_key) is None:
+                continue
             sc = inp[sc_key]
             new_sc = torch.empty_like(sc)
             new_sc[dst_t] = sc[src_t]

@@ -28,7 +28,7 @@ class _Li(ctypes.Structure):
         ("q", ctypes.c_void_p), ("q_scale", ctypes.c_void_p), ("w", ctypes.c_void_p),
         ("k_pool", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
         ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
-        ("q_start", ctypes.c_void_p)]
+        ("q_start", ctypes.c_void_p), ("q_sf", ctypes.c_void_p), ("k_sf", ctypes.c_void_p)]
 
 
 class _Sfa(ctypes.Structure):
@@ -77,7 +77,7 @@ def _li_struct(inp, keep):
     s.B, s.n_q, s.H_I, s.d_I, s.K = wl.B, wl.n_q, wl.H_I, wl.d_I, wl.K
     s.page_size, s.max_pages = wl.page_size, int(inp["pt_k"].shape[1])
     s.num_pages = int(inp["k_pool"].shape[0])
-    s.fp8 = 1 if wl.li_dtype == "fp8" else 0
+    s.fp8 = {"bf16": 0, "fp8": 1, "mxfp8": 2}[wl.li_dtype]
     s.q = keep.ptr(inp["q_li"])
     s.q_scale = keep.ptr(inp.get("q_scale"))
     s.w = keep.ptr(inp["w"])
@@ -86,6 +86,8 @@ def _li_struct(inp, keep):
     s.page_table = keep.ptr(inp["pt_k"])
     s.seq_lens = keep.ptr(inp["seq_lens"])
     s.q_start = keep.ptr(inp["q_start"])
+    s.q_sf = keep.ptr(inp.get("q_sf"))
+    s.k_sf = keep.ptr(inp.get("k_sf"))
     return s
 
 
@@ -157,6 +159,13 @@ def sfa(inp, idx, tokens=None):
 def decode_bf16(bits: int) -> float:
     f = lib().orc_bf16
     f.argtypes = [ctypes.c_uint16]
+    f.restype = ctypes.c_double
+    return f(bits)
+
+
+def decode_e8m0(bits: int) -> float:
+    f = lib().orc_e8m0
+    f.argtypes = [ctypes.c_uint8]
     f.restype = ctypes.c_double
     return f(bits)
 

@@ -26,7 +26,11 @@
  * Readings where the pages are silent (stated here and listed in the design notes):
  *   score      s(t,j) = sum_h w[t,h] * max(0, q[t,h,:] . k[j,:]); one key row per position,
  *              shared by all index heads; for e4m3 inputs q and k are the dequantised values
- *              q8 * q_scale[t,h] and k8 * k_scale[row].
+ *              q8 * q_scale[t,h] and k8 * k_scale[row]; for MXFP8 inputs ("Inference
+ *              Optimization for Kimi K3.1 Pro", section 4, fully quantised indexer path; "Day0
+ *              Inference Adaptation ... CANN", section 3.3: group size 32) every run of 32
+ *              consecutive elements of a q head or a key row shares one power-of-two scale, so
+ *              the dequantised value of element d is e4m3(q8[d]) * 2^(sf[d / 32] - 127).
  *   visibility a query token at absolute position p sees positions 0..p (itself included);
  *              the n new tokens of a sequence of length L sit at L-n .. L-1.
  *   selection  the first min(K, p+1) positions in the order (score descending, position
@@ -53,7 +57,8 @@
 
 typedef struct {
   int B, n_q, H_I, d_I, K, page_size, max_pages, num_pages;
-  int fp8;                    /* 0: bf16 q/k; 1: e4m3 q/k with fp32 scales            */
+  int fp8;                    /* 0: bf16 q/k; 1: e4m3 q/k with fp32 scales;
+                                 2: MXFP8 (e4m3 q/k with E8M0 scales per 32 elements)    */
   const void* q;              /* [n_q][H_I][d_I]                                        */
   const float* q_scale;       /* [n_q][H_I]          (fp8 only)                         */
   const float* w;             /* [n_q][H_I]                                             */
@@ -62,6 +67,8 @@ typedef struct {
   const int* page_table;      /* [B][max_pages]                                         */
   const int* seq_lens;        /* [B]                                                    */
   const int* q_start;         /* [B+1]                                                  */
+  const uint8_t* q_sf;        /* [n_q][H_I][d_I/32] E8M0   (MXFP8 only)                 */
+  const uint8_t* k_sf;        /* [num_pages][page_size][d_I/32] E8M0 (MXFP8 only)       */
 } orc_li;
 
 typedef struct {
@@ -95,6 +102,13 @@ double orc_e4m3(uint8_t bits) {
   return s ? -v : v;
 }
 
+/* OCP Microscaling E8M0 scale: an unsigned 8-bit exponent with bias 127, value 2^(e - 127);
+ * 0xFF is NaN. */
+double orc_e8m0(uint8_t bits) {
+  if (bits == 0xFF) return NAN;
+  return ldexp(1.0, (int)bits - 127);
+}
+
 /* ---- token -> (sequence, position) and position -> physical row ---------------------- */
 
 static int locate(const int* q_start, const int* seq_lens, int B, int t, int* b_out, int* p_out) {
@@ -119,12 +133,16 @@ static long long phys_row(const int* pt, int max_pages, int page_size, int b, in
 
 static double li_q(const orc_li* P, int t, int h, int d) {
   long long i = ((long long)t * P->H_I + h) * P->d_I + d;
+  if (P->fp8 == 2)
+    return orc_e4m3(((const uint8_t*)P->q)[i]) *
+           orc_e8m0(P->q_sf[((long long)t * P->H_I + h) * (P->d_I / 32) + d / 32]);
   if (P->fp8) return orc_e4m3(((const uint8_t*)P->q)[i]) * (double)P->q_scale[(long long)t * P->H_I + h];
   return orc_bf16(((const uint16_t*)P->q)[i]);
 }
 
 static double li_k(const orc_li* P, long long row, int d) {
   long long i = row * P->d_I + d;
+  if (P->fp8 == 2) return orc_e4m3(((const uint8_t*)P->k_pool)[i]) * orc_e8m0(P->k_sf[row * (P->d_I / 32) + d / 32]);
   if (P->fp8) return orc_e4m3(((const uint8_t*)P->k_pool)[i]) * (double)P->k_scale[row];
   return orc_bf16(((const uint16_t*)P->k_pool)[i]);
 }
@@ -154,7 +172,9 @@ static int li_check(const orc_li* P) {
       P->page_size <= 0 || P->max_pages <= 0 || !P->q || !P->w || !P->k_pool ||
       !P->page_table || !P->seq_lens || !P->q_start)
     return ORC_EARG;
-  if (P->fp8 && (!P->q_scale || !P->k_scale)) return ORC_EARG;
+  if (P->fp8 == 1 && (!P->q_scale || !P->k_scale)) return ORC_EARG;
+  if (P->fp8 == 2 && (!P->q_sf || !P->k_sf || P->d_I % 32 != 0)) return ORC_EARG;
+  if (P->fp8 < 0 || P->fp8 > 2) return ORC_EARG;
   for (int b = 0; b < P->B; ++b) {
     int L = P->seq_lens[b];
     if (L < 0 || (L + P->page_size - 1) / P->page_size > P->max_pages) return ORC_EARG;
@@ -312,4 +332,4 @@ int oracle_sfa(const orc_sfa* S, int n_tok, const int* toks, const int* idx, dou
   return err;
 }
 
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }

@@ -42,6 +42,38 @@ def li_problem(q, w, keys_by_pos, page_size, page_table, seq_len, n_new=1, K=4,
     return inp
 
 
+def li_problem_mx(q_blocks, w, k_blocks_by_pos, page_size, page_table, group, K=4):
+    """One sequence, one new token at the last position, MXFP8 inputs: q_blocks[h][g] and
+    k_blocks_by_pos[j][g] give the e4m3 code shared by all elements of group g and its E8M0
+    scale byte."""
+    H_I, n_grp = len(q_blocks), len(q_blocks[0])
+    d_I = n_grp * group
+    L = len(k_blocks_by_pos)
+    pages = (L + page_size - 1) // page_size
+    wl = di.Workload("hand_mx", [L], [1], H_I=H_I, d_I=d_I, K=K, H=1, li_dtype="mxfp8",
+                     page_size=page_size)
+    qc = torch.zeros((1, H_I, d_I), dtype=torch.uint8)
+    qsf = torch.zeros((1, H_I, n_grp), dtype=torch.uint8)
+    for h in range(H_I):
+        for g, blk in enumerate(q_blocks[h]):
+            qc[0, h, g * group:(g + 1) * group] = blk["code"]
+            qsf[0, h, g] = blk["sf"]
+    kc = torch.zeros((pages, page_size, d_I), dtype=torch.uint8)
+    ksf = torch.full((pages, page_size, n_grp), 127, dtype=torch.uint8)
+    for j, blocks in enumerate(k_blocks_by_pos):
+        pg, r = page_table[j // page_size], j % page_size
+        for g, blk in enumerate(blocks):
+            kc[pg, r, g * group:(g + 1) * group] = blk["code"]
+            ksf[pg, r, g] = blk["sf"]
+    return {"wl": wl, "pt_k": torch.tensor([page_table], dtype=torch.int32),
+            "seq_lens": torch.tensor([L], dtype=torch.int32),
+            "q_start": torch.tensor([0, 1], dtype=torch.int32),
+            "w": torch.tensor([w], dtype=torch.float32),
+            "q_li": qc.view(torch.float8_e4m3fn), "q_sf": qsf,
+            "k_pool": kc.view(torch.float8_e4m3fn), "k_sf": ksf,
+            "q_scale": None, "k_scale": None}
+
+
 def sfa_problem(q_heads, rows_by_pos, page_size, page_table, d_v, scale, n_new=1, K=2):
     """One sequence with len(rows_by_pos) positions; q_heads [H, d_qk] for every new token."""
     q = torch.tensor(q_heads, dtype=torch.float32)

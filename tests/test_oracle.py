@@ -15,7 +15,7 @@ import torch
 
 import dsa_inputs as di
 import oracle
-from oracle_cases import li_problem, sfa_problem
+from oracle_cases import li_problem, li_problem_mx, sfa_problem
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -176,6 +176,127 @@ def test_fp8_scores_equal_dequantised_bf16_scores():
     a = oracle.li_topk(inp)
     b = oracle.li_topk(inp8)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+
+
+# ---------------------------------------------------------------- indexer: MXFP8 inputs
+
+def test_e8m0_decoder_matches_its_definition_on_every_code():
+    """E8M0 (OCP Microscaling): 2^(code - 127), code 255 is NaN; torch's decoder where present."""
+    got = np.array([oracle.decode_e8m0(c) for c in range(256)])
+    assert np.isnan(got[255]) and not np.isnan(got[:255]).any()
+    assert all(got[c] == math.ldexp(1.0, c - 127) for c in range(255))
+    if hasattr(torch, "float8_e8m0fnu"):
+        ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu)
+        ref = ref.to(torch.float64).numpy()
+        assert np.array_equal(ref[:255], got[:255]) and np.isnan(ref[255])
+
+
+def _hand_mx(K=4):
+    g = _gold("li_mx_hand_example.json")
+    return g, li_problem_mx(g["q_blocks"], g["w"], g["k_blocks_by_position"], g["page_size"],
+                            g["page_table"], g["group"], K=K)
+
+
+def test_mx_hand_example_scores():
+    g, inp = _hand_mx()
+    s, _ = oracle.li_scores(inp, 0)
+    assert s.tolist() == g["scores"]
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4, 5, 6])
+def test_mx_hand_example_topk(K):
+    g, inp = _hand_mx(K=K)
+    idx, cnt, _ = oracle.li_topk(inp)
+    assert idx[0].tolist() == g["topk_full_context"][str(K)]
+    assert cnt[0] == min(K, 5)
+
+
+def _mx_dequant(codes, sf):
+    """Library decode (torch's e4m3) times 2^(sf - 127) repeated over each group of 32."""
+    v = codes.to(torch.float64)
+    e = sf.to(torch.int64) - 127
+    return v * torch.pow(2.0, e.to(torch.float64)).repeat_interleave(32, dim=-1)
+
+
+def test_mx_scores_match_library_matmul_on_integers():
+    """Integer e4m3 codes and scales in 2^-1..2^1 keep every sum exact: the oracle equals a torch
+    matmul of the library-dequantised logical keys with ReLU and the weights applied."""
+    inp = _random_li(15, d_I=64, li_dtype="mxfp8")
+    wl = inp["wl"]
+    assert set(torch.unique(inp["k_sf"]).tolist()) <= {126, 127, 128}
+    pt = inp["pt_k"]
+    for t, (b, p) in enumerate([(b, p) for b in range(wl.B)
+                                for p in range(wl.seq_lens[b] - wl.n_new[b], wl.seq_lens[b])]):
+        s, _ = oracle.li_scores(inp, t)
+        rows = [(int(pt[b, j // wl.page_size]), j % wl.page_size) for j in range(p + 1)]
+        keys = torch.stack([_mx_dequant(inp["k_pool"][a, r], inp["k_sf"][a, r]) for a, r in rows])
+        q = _mx_dequant(inp["q_li"][t], inp["q_sf"][t])          # [H_I, d_I]
+        dots = keys @ q.T
+        expect = (torch.clamp(dots, min=0) * inp["w"][t].to(torch.float64)).sum(1)
+        assert np.array_equal(s, expect.numpy())
+
+
+def test_mx_with_one_exponent_per_row_equals_per_token_fp8():
+    """When all groups of a query token (every head) share one exponent and all groups of a key
+    row share one, MXFP8 is the per-token/per-row scaled e4m3 format pinned above."""
+    inp = _random_li(16, d_I=64, li_dtype="mxfp8")
+    wl = inp["wl"]
+    g = torch.Generator().manual_seed(7)
+    eq = torch.randint(124, 131, (wl.n_q,), generator=g).to(torch.uint8)
+    ek = torch.randint(124, 131, tuple(inp["k_pool"].shape[:2]), generator=g).to(torch.uint8)
+    mx = dict(inp, q_sf=eq[:, None, None].expand(wl.n_q, wl.H_I, 2).contiguous(),
+              k_sf=ek[:, :, None].expand(*ek.shape, 2).contiguous())
+    wl8 = di.Workload(**{**wl.__dict__, "li_dtype": "fp8"})
+    f8 = dict(inp, wl=wl8, q_sf=None, k_sf=None,
+              q_scale=torch.pow(2.0, eq.double() - 127).float()[:, None].expand(wl.n_q, wl.H_I).contiguous(),
+              k_scale=torch.pow(2.0, ek.double() - 127).float().contiguous())
+    for t in range(wl.n_q):
+        assert np.array_equal(oracle.li_scores(mx, t)[0], oracle.li_scores(f8, t)[0])
+    a, b = oracle.li_topk(mx), oracle.li_topk(f8)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+
+
+@pytest.mark.parametrize("grp", [0, 1])
+def test_mx_group_scale_scales_only_its_own_group(grp):
+    """One head, unit weight, non-negative codes (so s is the dot product itself): doubling the
+    scale of group g of a key row adds exactly that group's share, which is what zeroing the
+    group's codes removes.  Doubling group g of the query does the same for every key."""
+    inp = _random_li(17, d_I=64, H_I=1, li_dtype="mxfp8")
+    wl = inp["wl"]
+    inp = dict(inp, q_li=inp["q_li"].float().abs().to(torch.float8_e4m3fn),
+               k_pool=inp["k_pool"].float().abs().to(torch.float8_e4m3fn),
+               w=torch.ones_like(inp["w"]))
+    t = wl.n_q - 1
+    s0, _ = oracle.li_scores(inp, t)
+    kz = inp["k_pool"].float().clone()
+    kz[..., grp * 32:(grp + 1) * 32] = 0
+    s_without, _ = oracle.li_scores(dict(inp, k_pool=kz.to(torch.float8_e4m3fn)), t)
+    share = s0 - s_without
+    assert np.all(share >= 0) and np.any(share > 0)
+    ksf = inp["k_sf"].clone()
+    ksf[..., grp] += 1
+    s_k, _ = oracle.li_scores(dict(inp, k_sf=ksf), t)
+    assert np.array_equal(s_k, s0 + share)
+    qsf = inp["q_sf"].clone()
+    qsf[t, :, grp] += 1
+    s_q, _ = oracle.li_scores(dict(inp, q_sf=qsf), t)
+    assert np.array_equal(s_q, s0 + share)
+
+
+def test_mx_generator_quantiser_follows_the_format():
+    """The input generator's MX quantiser: each group's largest code lies in [256, 448] (the
+    shared exponent is floor(log2 amax) - 8); codes below the clamp are within e4m3's half-ulp
+    (2^-4 relative) of x / 2^shared, clamped ones are +-448."""
+    x = torch.randn(6, 4, 128, generator=torch.Generator().manual_seed(3)).double()
+    q, sf = di._quant_mx(x.float())
+    codes = q.double()
+    assert codes.view(6, 4, 4, 32).abs().amax(-1).min() >= 256
+    assert codes.abs().max() <= 448
+    scaled = x / torch.pow(2.0, sf.double() - 127).repeat_interleave(32, -1)
+    clamped = scaled.abs() > 448
+    assert torch.all(codes[clamped].abs() == 448)
+    normal = ~clamped & (scaled.abs() >= 2.0 ** -6)
+    assert torch.all((codes - scaled).abs()[normal] <= scaled.abs()[normal] * 2.0 ** -4)
 
 
 # ---------------------------------------------------------------- top-K: definition by brute force
