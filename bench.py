@@ -55,9 +55,11 @@ def algorithmic(wl, cnt_total):
     """Per-step algorithmic work: key pages every token's visible range touches (read once per
     sequence), gathered latent rows (one 1152-byte row per selected index), FLOPs."""
     P = wl.page_size
-    elt = 1 if wl.li_dtype == "fp8" else 2
+    elt = 2 if wl.li_dtype == "bf16" else 1
     pages = sum(math.ceil(L / P) for L in wl.seq_lens)
-    k_bytes = pages * P * wl.d_I * elt + (pages * P * 4 if wl.li_dtype == "fp8" else 0)
+    # key scales: one fp32 per row (fp8), one E8M0 byte per 32 elements (mxfp8)
+    sc = {"bf16": 0, "fp8": 4, "mxfp8": wl.d_I // 32}[wl.li_dtype]
+    k_bytes = pages * P * (wl.d_I * elt + sc)
     gather_bytes = cnt_total * wl.d_qk * 2
     li_flop = 0
     for L, n in zip(wl.seq_lens, wl.n_new):
@@ -253,7 +255,8 @@ def run_ours(args):
     li_args = dsa.li_topk_args(inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"],
                                inp["q_start"], wl.K, q_scale=inp.get("q_scale"),
                                k_scale=inp.get("k_scale"), max_seq_len=ms, max_q_per_seq=mq,
-                               out_idx=idx, out_cnt=cnt, status=status)
+                               out_idx=idx, out_cnt=cnt, status=status, q_sf=inp.get("q_sf"),
+                               k_sf=inp.get("k_sf"))
     sfa_args = dsa.sfa_args(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"],
                             inp["q_start"], idx, softmax_scale=wl.softmax_scale, max_seq_len=ms,
                             max_q_per_seq=mq, out=out, lse=lse, status=status, workspace=ws)
@@ -327,7 +330,7 @@ def run_ours(args):
     # inputs arrive and step n-1's outputs leave while step n computes.
     e2e = None
     if not args.no_e2e:
-        names = [k for k in ["q_li", "q_scale", "w", "q_sfa", "pt_k", "pt_kv", "seq_lens", "q_start"]
+        names = [k for k in ["q_li", "q_scale", "q_sf", "w", "q_sfa", "pt_k", "pt_kv", "seq_lens", "q_start"]
                  if inp.get(k) is not None]
 
         def layout(specs):
@@ -355,7 +358,8 @@ def run_ours(args):
         li2 = [dsa.li_topk_args(d["q_li"], d["w"], inp["k_pool"], d["pt_k"], d["seq_lens"], d["q_start"],
                                 wl.K, q_scale=d.get("q_scale"), k_scale=inp.get("k_scale"),
                                 max_seq_len=ms, max_q_per_seq=mq, out_idx=o["idx"], out_cnt=o["cnt"],
-                                status=status) for d, o in zip(din, dout)]
+                                status=status, q_sf=d.get("q_sf"), k_sf=inp.get("k_sf"))
+               for d, o in zip(din, dout)]
         sfa2 = [dsa.sfa_args(d["q_sfa"], inp["kv_pool"], d["pt_kv"], d["seq_lens"], d["q_start"], o["idx"],
                              softmax_scale=wl.softmax_scale, max_seq_len=ms, max_q_per_seq=mq,
                              out=o["out"], lse=o["lse"], status=status, workspace=ws)
@@ -415,7 +419,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8" if wl.li_dtype == "fp8" else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.li_dtype,
         "data": "synthetic",
         "config": {**wl.describe(), "l2": "inputs larger than L2: every step streams %.0f MB of key pages "
                    "and gathers from a %.0f MB latent pool" % (work["k_bytes"] / 1e6,

@@ -27,7 +27,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK, DSA_ERR_TIMEOUT = range(6)
-DSA_BF16, DSA_FP8_E4M3 = 0, 1
+DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
 
 SYMBOLS = ["dsa_status_string", "dsa_last_error", "dsa_abi_version", "dsa_li_topk",
            "dsa_sfa_workspace_bytes", "dsa_sfa_decode", "dsa_sfa_prefill",
@@ -50,7 +50,7 @@ class LiArgs(ctypes.Structure):
         "B", "n_q", "H_I", "d_I", "K", "page_size", "max_pages", "num_pages", "max_seq_len",
         "max_q_per_seq", "dtype")] + [(n, ctypes.c_void_p) for n in (
             "q", "q_scale", "w", "k_pool", "k_scale", "page_table", "seq_lens", "q_start",
-            "out_idx", "out_cnt", "status")]
+            "out_idx", "out_cnt", "status", "q_sf", "k_sf")]
 
 
 class SfaArgs(ctypes.Structure):
@@ -134,8 +134,10 @@ def _host_max(seq_lens: torch.Tensor, q_start: torch.Tensor, max_seq_len, max_q_
 
 
 def li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_scale=None,
-                 max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None):
-    """Fill the C argument struct of dsa_li_topk (tensors must outlive the call)."""
+                 max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None,
+                 q_sf=None, k_sf=None):
+    """Fill the C argument struct of dsa_li_topk (tensors must outlive the call).  e4m3 q/k take
+    either fp32 q_scale/k_scale (FP8) or uint8 E8M0 group scales q_sf/k_sf (MXFP8)."""
     fp8 = q.dtype == torch.float8_e4m3fn
     n_q, H_I, d_I = q.shape
     max_seq_len, max_q_per_seq = _host_max(seq_lens, q_start, max_seq_len, max_q_per_seq)
@@ -146,16 +148,17 @@ def li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None
     a.max_pages = page_table.shape[1]
     a.num_pages = k_pool.shape[0]
     a.max_seq_len, a.max_q_per_seq = max_seq_len, max_q_per_seq
-    a.dtype = DSA_FP8_E4M3 if fp8 else DSA_BF16
+    a.dtype = (DSA_MXFP8_E4M3 if q_sf is not None else DSA_FP8_E4M3) if fp8 else DSA_BF16
     a.q, a.q_scale, a.w, a.k_pool, a.k_scale = _ptr(q), _ptr(q_scale), _ptr(w), _ptr(k_pool), _ptr(k_scale)
     a.page_table, a.seq_lens, a.q_start = _ptr(page_table), _ptr(seq_lens), _ptr(q_start)
     a.out_idx, a.out_cnt, a.status = _ptr(out_idx), _ptr(out_cnt), _ptr(status)
+    a.q_sf, a.k_sf = _ptr(q_sf), _ptr(k_sf)
     return a
 
 
 def li_topk(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_scale=None,
             max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None,
-            stream=None):
+            stream=None, q_sf=None, k_sf=None):
     """Fused indexer scoring + top-K.  Returns (idx [n_q, K] int32, cnt [n_q] int32)."""
     lib = load()
     n_q = q.shape[0]
@@ -165,7 +168,7 @@ def li_topk(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_s
         out_cnt = torch.empty((n_q,), dtype=torch.int32, device=q.device)
     a = li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, q_scale=q_scale,
                      k_scale=k_scale, max_seq_len=max_seq_len, max_q_per_seq=max_q_per_seq,
-                     out_idx=out_idx, out_cnt=out_cnt, status=status)
+                     out_idx=out_idx, out_cnt=out_cnt, status=status, q_sf=q_sf, k_sf=k_sf)
     _check(lib.dsa_li_topk(ctypes.byref(a), _stream(stream)), "dsa_li_topk")
     return out_idx, out_cnt
 
@@ -285,7 +288,7 @@ def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=
     idx, cnt = li_topk(inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"],
                        inp["q_start"], wl.K, q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"),
                        max_seq_len=ms, max_q_per_seq=mq, out_idx=idx, out_cnt=cnt, status=status,
-                       stream=stream)
+                       stream=stream, q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf"))
     f = sfa_prefill if prefill else sfa_decode
     out, lse = f(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"], inp["q_start"], idx,
                  softmax_scale=inp["softmax_scale"], max_seq_len=ms, max_q_per_seq=mq, out=out,

@@ -112,7 +112,7 @@ int dsa_abi_version(void) { return DSA_ABI_VERSION; }
 
 size_t dsa_page_bytes(dsa_dtype dtype, int rows, int dim) {
   if (rows < 0 || dim < 0) return 0;
-  const size_t elt = dtype == DSA_BF16 ? 2 : (dtype == DSA_FP8_E4M3 ? 1 : 0);
+  const size_t elt = dtype == DSA_BF16 ? 2 : ((dtype == DSA_FP8_E4M3 || dtype == DSA_MXFP8_E4M3) ? 1 : 0);
   return elt * (size_t)rows * (size_t)dim;
 }
 
@@ -151,13 +151,16 @@ dsa_status dsa_li_topk(const dsa_li_args* a, dsa_stream_t stream) {
   if (a->B <= 0 || a->n_q < 0 || a->K <= 0 || a->max_pages <= 0 || a->num_pages <= 0 ||
       a->H_I <= 0 || a->d_I <= 0)
     return fail(DSA_ERR_INVALID_ARG, "li_topk: non-positive size");
-  if (a->dtype != DSA_BF16 && a->dtype != DSA_FP8_E4M3)
+  if (a->dtype != DSA_BF16 && a->dtype != DSA_FP8_E4M3 && a->dtype != DSA_MXFP8_E4M3)
     return fail(DSA_ERR_INVALID_ARG, "li_topk: unknown dtype");
   if (a->n_q == 0) return DSA_OK;
   if (!a->q || !a->w || !a->k_pool || !a->page_table || !a->seq_lens || !a->q_start || !a->out_idx)
     return fail(DSA_ERR_INVALID_ARG, "li_topk: null device pointer");
   if (a->dtype == DSA_FP8_E4M3 && (!a->q_scale || !a->k_scale))
     return fail(DSA_ERR_INVALID_ARG, "li_topk: FP8 needs q_scale and k_scale");
+  if (a->dtype == DSA_MXFP8_E4M3 &&
+      (!a->q_sf || !a->k_sf || ((reinterpret_cast<uintptr_t>(a->q_sf) | reinterpret_cast<uintptr_t>(a->k_sf)) & 3u) != 0))
+    return fail(DSA_ERR_INVALID_ARG, "li_topk: MXFP8 needs 4-byte aligned q_sf and k_sf");
   if (a->max_seq_len <= 0 || a->max_q_per_seq <= 0 || a->max_q_per_seq > a->n_q)
     return fail(DSA_ERR_INVALID_ARG, "li_topk: max_seq_len / max_q_per_seq out of range");
   if ((long long)a->max_seq_len > (long long)a->max_pages * a->page_size)

@@ -65,9 +65,11 @@ struct Params {
   int* status;
   const void* q;       // raw pointers (used by the CUDA-core scoring variant only)
   const void* k_pool;
+  const uint8_t* q_sf;  // MXFP8: E8M0 scales of 32-element groups, [n_q][H_I][D_I/32]
+  const uint8_t* k_sf;  //        and [num_pages][64][D_I/32]
 };
 
-template <int D_I, bool FP8, int H_I, int T>
+template <int D_I, bool FP8, int H_I, int T, bool MX = false>
 struct Cfg {
   static constexpr int kElt = FP8 ? 1 : 2;
   static constexpr int kRowBytes = D_I * kElt;      // 128 or 256
@@ -76,12 +78,21 @@ struct Cfg {
   static constexpr int kNCol = (T * H_I < 16) ? 16 : T * H_I;  // MMA N (>= 16 for M = 128)
   static constexpr int kTileBytes = kTileKeys * kRowBytes;
   static constexpr int kQBytes = kNCol * kRowBytes;
-  static constexpr int kTmemCols = (2 * kNCol <= 32)    ? 32
-                                   : (2 * kNCol <= 64)  ? 64
-                                   : (2 * kNCol <= 128) ? 128
-                                   : (2 * kNCol <= 256) ? 256
+  // MXFP8: the E8M0 scale cells follow the two accumulators.  Key side (MMA operand A) of
+  // accumulator a: columns kSfA + 4a .. +3, key r of the tile at lane r, column kSfA + 4a + r/32
+  // (each lane quadrant reads its own column); query side (operand B): columns kSfB + n/32, MMA
+  // column n at lane n%32 of every lane quadrant.  Byte g of a cell is the scale of group g.
+  static constexpr int kSfA = 2 * kNCol;
+  static constexpr int kSfB = kSfA + 8;
+  static constexpr int kTmemNeed = 2 * kNCol + (MX ? 8 + (kNCol + 31) / 32 : 0);
+  static constexpr int kTmemCols = (kTmemNeed <= 32)    ? 32
+                                   : (kTmemNeed <= 64)  ? 64
+                                   : (kTmemNeed <= 128) ? 128
+                                   : (kTmemNeed <= 256) ? 256
                                                         : 512;
   static_assert(kNCol % 16 == 0 && kNCol <= 256, "MMA N");
+  static_assert(kTmemNeed <= 512, "tensor memory columns");
+  static_assert(!MX || (FP8 && D_I == 128), "MXFP8: e4m3 elements, four 32-element groups per row");
   static_assert(T * H_I <= 256, "tokens x heads per group");
 };
 
@@ -107,6 +118,7 @@ struct Ctl {
   uint64_t tempty[2];
   uint64_t qbar;
   uint64_t drain;
+  uint64_t sinit;  // MXFP8: the first scale cells are in tensor memory
   uint32_t tmem_base;
   int abort;
   uint32_t scan[kThreads / 32];
@@ -230,11 +242,11 @@ DSA_DEV float e4m3_to_float(uint8_t b) {
 
 // ---- the fused kernel ----
 
-template <int D_I, bool FP8, int H_I, int T, bool kTensorCore>
+template <int D_I, bool FP8, int H_I, int T, bool kTensorCore, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     li_topk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const Params p) {
-  using CF = Cfg<D_I, FP8, H_I, T>;
+  using CF = Cfg<D_I, FP8, H_I, T, MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -285,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->qbar, 1);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->sinit, 256);  // both epilogue groups
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -311,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float v = 0.f;
     if (tt < nt) {
       v = p.w[(size_t)(t0 + tt) * H_I + h];
-      if (FP8) v *= p.q_scale[(size_t)(t0 + tt) * H_I + h];
+      if (FP8 && !MX) v *= p.q_scale[(size_t)(t0 + tt) * H_I + h];  // per-token FP8 scale
     }
     wts[i] = v;
   }
@@ -365,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(q_s);
       const uint32_t st_addr = smem_u32(stage_base);
       bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
+      if constexpr (MX) ok = ok && mbar_wait(&ctl->sinit, 0, abort, p.status);
       for (int i = 0; ok && i < ntile; ++i) {
         const int s = i % p.nstage;
         const uint32_t ph = (uint32_t)(i / p.nstage) & 1u;
@@ -379,7 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t box = (uint32_t)(kk * 32) / 128u, off = (uint32_t)(kk * 32) % 128u;
           const uint64_t ad = sdesc_sw128(st_addr + (uint32_t)s * CF::kTileBytes + box * 16384u + off, 16, 1024);
           const uint64_t bd = sdesc_sw128(q_addr + box * (uint32_t)(CF::kNCol * 128) + off, 16, 1024);
-          if (FP8)
+          if constexpr (MX)  // K step kk = scale group kk (byte kk of every scale cell)
+            mma_mx_ss(d, ad, bd, idesc_mx_e4m3(128, CF::kNCol, kk, kk),
+                      tmem + (uint32_t)(CF::kSfA + 4 * a), tmem + (uint32_t)CF::kSfB, kk > 0 ? 1u : 0u);
+          else if (FP8)
             mma_f8_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
           else
             mma_f16_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
@@ -396,18 +413,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int grp = (warp - 4) >> 2;
       const int qd = warp & 3;  // TMEM lane quadrant of this warp
       const int row = qd * 32 + lane;
+      const uint32_t lanes = tmem + ((uint32_t)(qd * 32) << 16);
+      constexpr uint32_t kSfOne = 0x7F7F7F7Fu;  // four E8M0 scales of 1
+      // MXFP8: the four group scales of key `row` of tile i (one 32-bit word per key row)
+      auto key_sf = [&](int i) -> uint32_t {
+        const int pg = pages[2 * i + (row >> 6)];
+        return pg >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(p.k_sf) + (size_t)pg * 64 + (row & 63))
+                       : kSfOne;
+      };
+      if constexpr (MX) {
+        // Scale cells of this group's first tile and (group 0) of the query heads, before the
+        // first MMA; later tiles' key scales are written while the previous tile of the same
+        // accumulator is reduced (below).
+        tmem_st_x1(lanes + (uint32_t)(CF::kSfA + 4 * grp + qd), grp < ntile ? key_sf(grp) : kSfOne);
+        if (grp == 0) {
+          for (int c = 0; c * 32 < CF::kNCol; ++c) {
+            const int n = c * 32 + lane, tt = n / H_I, h = n % H_I;
+            uint32_t v = kSfOne;
+            if (n < T * H_I && t0 + tt < p.n_q)
+              v = __ldg(reinterpret_cast<const uint32_t*>(p.q_sf) + (size_t)(t0 + tt) * H_I + h);
+            tmem_st_x1(lanes + (uint32_t)(CF::kSfB + c), v);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&ctl->sinit);
+      }
       for (int i = grp; i < ntile; i += 2) {
         const int a = grp;
         const int j = lo + i * kTileKeys + row;
         float ks = 1.f;
-        if (FP8) {
+        if (FP8 && !MX) {
           const int pg = pages[2 * i + (row >> 6)];
           ks = pg >= 0 ? p.k_scale[(size_t)pg * 64 + (row & 63)] : 0.f;
         }
+        const uint32_t sf_next = (MX && i + 2 < ntile) ? key_sf(i + 2) : kSfOne;
         const bool ok = mbar_wait(&ctl->tfull[a], (uint32_t)(i >> 1) & 1u, abort, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;  // tcgen05.ld below needs the whole warp
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(a * CF::kNCol);
+        // MMA i has completed, so its scale cells are free: fill them for tile i + 2
+        if constexpr (MX) tmem_st_x1(lanes + (uint32_t)(CF::kSfA + 4 * a + qd), sf_next);
+        const uint32_t taddr = lanes + (uint32_t)(a * CF::kNCol);
 #pragma unroll 1
         for (int tt = 0; tt < T; ++tt) {
           float s;
@@ -440,12 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             s = a0 + a1;
           }
-          if (FP8) s *= ks;
+          if (FP8 && !MX) s *= ks;
           const bool valid = tt < nt && j < lo + p.chunk && j <= pos0 + tt;
           const uint32_t u = valid ? score_key(s) : 0u;
           scores[tt * p.chunk + (j - lo)] = u;
           if (valid) atomicAdd(&hist[tt * kHistWords + (u >> 22)], 1u << (((u >> 21) & 1u) * 16u));
         }
+        if constexpr (MX) tmem_st_wait();  // the scale cells of tile i + 2 are written
         tc_fence_before();
         mbar_arrive(&ctl->tempty[a]);
       }
@@ -457,16 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pg = pages[e >> 6];
       const size_t row = (size_t)(pg < 0 ? 0 : pg) * 64 + (j & 63);
       float ks = 1.f;
-      if (FP8) ks = p.k_scale[row];
+      if (FP8 && !MX) ks = p.k_scale[row];
       for (int tt = 0; tt < T; ++tt) {
         float s = 0.f;
-        for (int h = 0; h < H_I; ++h) {
+        for (int h = 0; tt < nt && h < H_I; ++h) {  // tokens of the group only (t0 + tt < n_q)
           float dot = 0.f;
           for (int d = 0; d < D_I; ++d) {
             float qv, kv;
             if (FP8) {
               qv = e4m3_to_float(((const uint8_t*)p.q)[((size_t)(t0 + tt) * H_I + h) * D_I + d]);
               kv = e4m3_to_float(((const uint8_t*)p.k_pool)[row * D_I + d]);
+              if (MX) {
+                qv = ldexpf(qv, (int)p.q_sf[((size_t)(t0 + tt) * H_I + h) * (D_I / 32) + d / 32] - 127);
+                kv = ldexpf(kv, (int)p.k_sf[row * (D_I / 32) + d / 32] - 127);
+              }
             } else {
               qv = bf16_bits_to_float(((const uint16_t*)p.q)[((size_t)(t0 + tt) * H_I + h) * D_I + d]);
               kv = bf16_bits_to_float(((const uint16_t*)p.k_pool)[row * D_I + d]);
@@ -475,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           s = fmaf(wts[tt * H_I + h], fmaxf(dot, 0.f), s);
         }
-        if (FP8) s *= ks;
+        if (FP8 && !MX) s *= ks;
         const bool valid = tt < nt && pg >= 0 && j <= pos0 + tt;
         const uint32_t u = valid ? score_key(s) : 0u;
         scores[tt * p.chunk + e] = u;
@@ -1054,16 +1105,16 @@ static bool use_cuda_core_scores() {
   return e && e[0] == '1';
 }
 
-template <int D_I, bool FP8, int H_I, int T>
+template <int D_I, bool FP8, int H_I, int T, bool MX = false>
 static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::string& err) {
-  using CF = Cfg<D_I, FP8, H_I, T>;
+  using CF = Cfg<D_I, FP8, H_I, T, MX>;
   DeviceInfo dev;
   if (!device_info(dev, err)) return DSA_ERR_CUDA;
   const int groups = (a.max_q_per_seq + T - 1) / T;
   const int maxL = std::max(a.max_seq_len, 1);
 
   const bool simple = use_cuda_core_scores();
-  auto kern = simple ? li_topk_kernel<D_I, FP8, H_I, T, false> : li_topk_kernel<D_I, FP8, H_I, T, true>;
+  auto kern = simple ? li_topk_kernel<D_I, FP8, H_I, T, false, MX> : li_topk_kernel<D_I, FP8, H_I, T, true, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: set shared memory size", err);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1167,6 +1218,8 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.status = a.status;
   p.q = a.q;
   p.k_pool = a.k_pool;
+  p.q_sf = a.q_sf;
+  p.k_sf = a.k_sf;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(best_c * a.B * groups));
@@ -1203,7 +1256,12 @@ dsa_status launch_li_topk(const dsa_li_args& a, cudaStream_t stream, std::string
 
 static dsa_status launch_li_topk_T(const dsa_li_args& a, int T, cudaStream_t stream, std::string& err) {
   const bool fp8 = a.dtype == DSA_FP8_E4M3;
+  const bool mx = a.dtype == DSA_MXFP8_E4M3;
   if (a.H_I == 64 && a.d_I == 128) {
+    if (mx) {  // at most 2 tokens per group: the scale cells need tensor memory beside 2 x 128 columns
+      if (T == 1) return li::launch_impl<128, true, 64, 1, true>(a, stream, err);
+      return li::launch_impl<128, true, 64, 2, true>(a, stream, err);
+    }
     if (fp8) {
       if (T == 1) return li::launch_impl<128, true, 64, 1>(a, stream, err);
       if (T == 2) return li::launch_impl<128, true, 64, 2>(a, stream, err);
@@ -1213,13 +1271,13 @@ static dsa_status launch_li_topk_T(const dsa_li_args& a, int T, cudaStream_t str
     if (T == 2) return li::launch_impl<128, false, 64, 2>(a, stream, err);
     return li::launch_impl<128, false, 64, 4>(a, stream, err);
   }
-  if (a.H_I == 8 && a.d_I == 64 && !fp8) {
+  if (a.H_I == 8 && a.d_I == 64 && !fp8 && !mx) {
     if (T == 1) return li::launch_impl<64, false, 8, 1>(a, stream, err);
     if (T == 2) return li::launch_impl<64, false, 8, 2>(a, stream, err);
     return li::launch_impl<64, false, 8, 4>(a, stream, err);
   }
   err = "li_topk: unsupported (H_I, d_I, dtype) = (" + std::to_string(a.H_I) + ", " +
-        std::to_string(a.d_I) + ", " + (fp8 ? "fp8" : "bf16") + ")";
+        std::to_string(a.d_I) + ", " + (mx ? "mxfp8" : fp8 ? "fp8" : "bf16") + ")";
   return DSA_ERR_UNSUPPORTED;
 }
 

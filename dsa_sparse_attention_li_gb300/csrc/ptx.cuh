@@ -256,6 +256,20 @@ DSA_DEV void mma_f8_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t ides
       : "memory");
 }
 
+// MXFP8 (kind::mxf8f6f4, e4m3 A/B, E8M0 scale per 32 K elements), fp32 accumulate.  One MMA
+// covers K = 32, i.e. one scale per row of A and per column of B, read from tensor memory:
+// sfa holds A's scales (row r at lane r, column sfa + r/32), sfb B's (column n at lane
+// 32*q + n%32 of every lane quadrant q, column sfb + n/32); the instruction descriptor picks
+// the byte of each 32-bit cell.
+DSA_DEV void mma_mx_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa,
+                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every MMA issued so far by this thread has completed.
 DSA_DEV void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -274,6 +288,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major 
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+
+// kind::mxf8f6f4 with e4m3 A/B, E8M0 scales (bit 23), fp32 D; sf_a / sf_b select the byte of
+// the 32-bit scale cell used for A and for B.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, int sf_a, int sf_b) {
+  return ((uint32_t)sf_b << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_a << 29);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.  K-major operands: rows of 128 B, 8-row
@@ -332,6 +353,10 @@ DSA_DEV void tmem_ld_x32(uint32_t taddr, uint32_t* r) {
 }
 
 DSA_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+DSA_DEV void tmem_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 
 DSA_DEV void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
   asm volatile(

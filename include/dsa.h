@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -55,7 +55,8 @@ typedef enum {
   DSA_ERR_TIMEOUT = 5       /* (in *status) a bounded device-side wait gave up                */
 } dsa_status;
 
-typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1 } dsa_dtype;
+/* DSA_MXFP8_E4M3: e4m3 elements with one E8M0 (power-of-two) scale per 32 consecutive elements. */
+typedef enum { DSA_BF16 = 0, DSA_FP8_E4M3 = 1, DSA_MXFP8_E4M3 = 2 } dsa_dtype;
 
 /* Human-readable name of a status code (static storage). */
 const char* dsa_status_string(dsa_status s);
@@ -74,11 +75,16 @@ int dsa_abi_version(void);
  * For every query token t (at position p):
  *   s(t, j) = sum_{h < H_I} w[t][h] * max(0, q[t][h][:] . k[j][:])      for 0 <= j <= p,
  * with one index key row k[j] (d_I wide) per position, shared by all index heads; in FP8 mode
- * q[t][h][:] = q8 * q_scale[t][h] and k[j][:] = k8 * k_scale[row(j)].  The selected set is the
+ * q[t][h][:] = q8 * q_scale[t][h] and k[j][:] = k8 * k_scale[row(j)]; in MXFP8 mode
+ * ("Inference Optimization for Kimi K3.1 Pro", section 4: the indexer's fully quantised path,
+ * group size 32) q[t][h][d] = q8 * 2^(q_sf[t][h][d/32] - 127) and
+ * k[j][d] = k8 * 2^(k_sf[row(j)][d/32] - 127) (E8M0 bytes; 255 is not a valid scale).  The
+ * selected set is the
  * first min(K, p+1) positions in the order (score descending, position ascending) -- ties go to
  * the lower position, and -0.0 equals +0.0.  Scores never leave the chip.
  *
- * Supported: page_size 64; (H_I, d_I) in {(8, 64), (64, 128)}; dtype BF16 or FP8_E4M3 (d_I 128);
+ * Supported: page_size 64; (H_I, d_I) in {(8, 64), (64, 128)}; dtype BF16, or FP8_E4M3 and
+ * MXFP8_E4M3 with (H_I, d_I) = (64, 128);
  * 1 <= K <= 2048; max_seq_len <= 131072; any number of tokens per sequence (decode, speculative
  * multi-token decode, chunked prefill).
  */
@@ -104,6 +110,9 @@ typedef struct {
   int32_t* out_idx;       /* [n_q][K] selected positions, ascending, then -1 padding      */
   int32_t* out_cnt;       /* [n_q] number selected = min(K, p+1), or NULL                 */
   int32_t* status;        /* device int32 error word, or NULL                             */
+  const uint8_t* q_sf;    /* [n_q][H_I][d_I/32] E8M0 group scales, MXFP8 only (else NULL) */
+  const uint8_t* k_sf;    /* [num_pages][page_size][d_I/32] E8M0, MXFP8 only; the 4-byte
+                             row of scales must be 4-byte aligned (d_I = 128)              */
 } dsa_li_args;
 
 dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
@@ -186,7 +195,8 @@ dsa_status dsa_sfa_decode_static(const dsa_sfa_args* args, dsa_stream_t stream);
 /* Cache layout and page-table helpers                                                         */
 /* ------------------------------------------------------------------------------------------ */
 
-/* Bytes of one page of `rows` rows of `dim` elements of `dtype` (0 on invalid input). */
+/* Bytes of one page of `rows` rows of `dim` elements of `dtype` (0 on invalid input); for
+ * MXFP8 the elements only (the E8M0 scales are a separate [rows][dim/32] byte array). */
 size_t dsa_page_bytes(dsa_dtype dtype, int rows, int dim);
 
 /*

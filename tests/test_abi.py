@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     lib = dsa.load()
-    assert lib.dsa_abi_version() == 1
+    assert lib.dsa_abi_version() == 2
     assert dsa.status_string(0) == "DSA_OK"
     assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
     assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"
@@ -37,7 +37,7 @@ def test_abi_version_and_status_strings():
 
 def test_struct_layouts_match_header():
     """ctypes mirrors of the argument structs have the C sizes (x86_64 / aarch64 LP64)."""
-    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 11 * 8
+    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 13 * 8
     assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8
 
 

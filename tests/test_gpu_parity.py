@@ -70,6 +70,30 @@ def test_fp8_normal_small(cuda_lib):
     check_sfa(inp_cpu, g, toks)
 
 
+@pytest.mark.parametrize("lens,new", [([6000, 2500, 300], [1, 2, 1]), ([4100, 129], [1, 1]),
+                                      ([3000], [9])])
+def test_mxfp8_integer_unit_case_bit_exact(cuda_lib, lens, new):
+    """MXFP8: integer e4m3 codes with group scales 2^-1..2^1 keep every fp32 step exact."""
+    inp_cpu, inp = _small("decode_32k_mxfp8", seq_lens=lens, n_new=new, values="int4",
+                          w_values="int14")
+    assert set(torch.unique(inp_cpu["k_sf"]).tolist()) == {126, 127, 128}
+    g = run_gpu(inp, prefill=False)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    n_exact, _ = check_indices(inp_cpu, g, toks, exact=True)
+    assert n_exact == len(toks)
+
+
+@pytest.mark.parametrize("lens,new", [([7000, 3100], [1, 2]), ([5000], [40])])
+def test_mxfp8_normal_small(cuda_lib, lens, new):
+    inp_cpu, inp = _small("decode_32k_mxfp8", seq_lens=lens, n_new=new)
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = sample_tokens(inp_cpu["wl"], 12, seed=2)
+    check_indices(inp_cpu, g, toks, exact=False)
+    check_sfa(inp_cpu, g, toks)
+
+
 def test_prefill_small(cuda_lib):
     inp_cpu, inp = _small("prefill_64k", seq_lens=[3000], n_new=[300], K=256)
     g = run_gpu(inp, prefill=True)
@@ -222,7 +246,8 @@ def test_cuda_graph_replay_matches_eager(cuda_lib):
 # ------------------------------------------------------------------ full-size workloads
 
 FULL = [("decode_int_4k", True, BF16_TOL), ("decode_32k", False, BF16_TOL),
-        ("decode_32k_fp8", False, FP8_TOL), ("specdec_ragged", False, BF16_TOL),
+        ("decode_32k_fp8", False, FP8_TOL), ("decode_32k_mxfp8", False, FP8_TOL),
+        ("specdec_ragged", False, BF16_TOL),
         ("prefill_64k", False, BF16_TOL)]
 
 
