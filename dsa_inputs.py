@@ -57,6 +57,8 @@ class Workload:
     d_v: int = D_V
     page_size: int = PAGE
     softmax_scale: float = field(default=1.0 / math.sqrt(D_QK))
+    d_q: int = 1536                 # Indexer Prolog: input width of the Q projection
+    d_model: int = 7168             # Indexer Prolog: input width of the K / head-weight projections
 
     @property
     def B(self) -> int:
@@ -102,6 +104,8 @@ def preset(name: str) -> Workload:
     decode_32k      : 32 sequences x 1 token, L=32768, 64x128 index heads, K=2048, 128 heads
     decode_32k_fp8  : decode_32k with e4m3 index q/k and per-token fp32 scales
     decode_32k_mxfp8: decode_32k with MXFP8 index q/k (e4m3 elements, one E8M0 scale per 32)
+    prolog_decode_32k: the Indexer Prolog of decode_32k_mxfp8's 32 new tokens (Q projection from
+                      a 1536-wide query input, K and head weights from a 7168-wide hidden state)
     specdec_ragged  : 64 sequences x 2 tokens (verified + draft), L log-uniform in [1024, 131072]
     prefill_64k     : 1 sequence, 4096 new tokens appended to a 61440-token prefix
     """
@@ -116,6 +120,9 @@ def preset(name: str) -> Workload:
     if name == "decode_32k_mxfp8":
         return Workload(name, [32768] * 32, [1] * 32, H_I=64, d_I=128, K=2048, H=128,
                         li_dtype="mxfp8", seed=1006)
+    if name == "prolog_decode_32k":
+        return Workload(name, [32768] * 32, [1] * 32, H_I=64, d_I=128, K=2048, H=128,
+                        li_dtype="mxfp8", seed=1007)
     if name == "specdec_ragged":
         lens = _log_uniform_lengths(64, 1024, 131072, seed=1004)
         return Workload(name, lens, [2] * 64, H_I=64, d_I=128, K=2048, H=128, seed=1004)
@@ -271,6 +278,60 @@ def generate(wl: Workload, device="cpu") -> dict:
         qs_.append(qs_[-1] + n)
     out["q_start"] = torch.tensor(qs_, dtype=torch.int32, device=device)
     out["softmax_scale"] = wl.softmax_scale
+    return out
+
+
+def generate_prolog(wl: Workload, device="cpu") -> dict:
+    """Inputs of the Indexer Prolog for the new tokens of ``wl``: activations, random projection
+    weights (the model's weights are not available; the prolog's arithmetic does not depend on
+    their values), LayerNorm parameters, and a key cache (random contents) with its page table,
+    into which the prolog writes the new tokens' keys.
+
+    values "normal": x ~ N(0, 1), weights ~ N(0, 1/fan_in), gamma ~ 1 + N(0, 0.1^2),
+    beta ~ N(0, 0.1^2).  values "int4": x and weights integers in [-2, 2], gamma 1, beta 0 (every
+    projection is then exact in fp32)."""
+    device = torch.device(device)
+    gs = torch.Generator().manual_seed(wl.seed)
+    gv = torch.Generator(device=device).manual_seed(wl.seed + 15485863)
+    n_q, F = wl.n_q, wl.H_I * wl.d_I
+
+    def draw(shape, fan_in):
+        if wl.values == "int4":
+            return torch.randint(-2, 3, shape, generator=gv, device=device).to(torch.bfloat16)
+        return (torch.randn(shape, generator=gv, device=device) / math.sqrt(fan_in)).to(torch.bfloat16)
+
+    out = {"wl": wl}
+    out["xq"] = draw((n_q, wl.d_q), 1)
+    out["x"] = draw((n_q, wl.d_model), 1)
+    out["w_q"] = draw((F, wl.d_q), wl.d_q)
+    out["w_k"] = draw((wl.d_I, wl.d_model), wl.d_model)
+    out["w_w"] = draw((wl.H_I, wl.d_model), wl.d_model)
+    if wl.values == "int4":
+        out["ln_gamma"] = torch.ones(wl.d_I, device=device)
+        out["ln_beta"] = torch.zeros(wl.d_I, device=device)
+    else:
+        out["ln_gamma"] = 1 + 0.1 * torch.randn(wl.d_I, generator=gv, device=device)
+        out["ln_beta"] = 0.1 * torch.randn(wl.d_I, generator=gv, device=device)
+    out["ln_eps"] = 1e-6
+    out["w_scale"] = 1.0 / math.sqrt(wl.H_I)
+    pt_k = _page_table(wl.pages(), wl.max_pages, gs)
+    out["pt_k"] = pt_k.to(device)
+    rows = wl.num_pages * wl.page_size
+    if wl.li_dtype == "mxfp8":
+        codes = torch.randint(0, 256, (rows, wl.d_I), generator=gv, device=device).to(torch.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0  # no NaN codes in the old contents
+        out["k_pool"] = codes.view(torch.float8_e4m3fn).view(wl.num_pages, wl.page_size, wl.d_I)
+        out["k_sf"] = torch.randint(120, 135, (wl.num_pages, wl.page_size, wl.d_I // MX_GROUP),
+                                    generator=gv, device=device).to(torch.uint8)
+    else:
+        out["k_pool"] = torch.randn((wl.num_pages, wl.page_size, wl.d_I), generator=gv,
+                                    device=device).to(torch.bfloat16)
+        out["k_sf"] = None
+    out["seq_lens"] = torch.tensor(wl.seq_lens, dtype=torch.int32, device=device)
+    qs_ = [0]
+    for n in wl.n_new:
+        qs_.append(qs_[-1] + n)
+    out["q_start"] = torch.tensor(qs_, dtype=torch.int32, device=device)
     return out
 
 

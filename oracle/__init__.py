@@ -9,6 +9,8 @@ Functions:
   li_scores(inp, t)          -> (s[0..p], mag[0..p]) float64 for query token t
   li_topk(inp, tokens)       -> (idx [n, K] int32, cnt [n] int32, kth [n] float64)
   sfa(inp, idx, tokens)      -> (out [n, H, d_v] float64, lse [n, H] float64)
+  prolog(inp)                -> Indexer Prolog outputs (projections, LayerNorm, quantisation)
+  mx_quantize(v)             -> OCP MX e4m3 codes and E8M0 scale bytes of a vector
 ``inp`` is the dict produced by ``dsa_inputs.generate`` (tensors moved to the CPU on demand).
 """
 import ctypes
@@ -154,6 +156,58 @@ def sfa(inp, idx, tokens=None):
     if rc != 0:
         raise ValueError("oracle_sfa failed: %d" % rc)
     return out, lse
+
+
+class _Prolog(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_q", "B", "d_q", "d_model", "H_I", "d_I", "mx")] + [
+        (n, ctypes.c_void_p) for n in ("xq", "x", "w_q", "w_k", "w_w", "ln_gamma", "ln_beta")] + [
+        ("ln_eps", ctypes.c_double), ("w_scale", ctypes.c_double), ("page_table", ctypes.c_void_p),
+        ("max_pages", ctypes.c_int), ("page_size", ctypes.c_int), ("seq_lens", ctypes.c_void_p),
+        ("q_start", ctypes.c_void_p)]
+
+
+def prolog(inp):
+    """Indexer Prolog of every new token (``inp`` from ``dsa_inputs.generate_prolog``).  Returns
+    q_val [n_q, H_I*d_I], k_val [n_q, d_I] (fp64 before rounding), w [n_q, H_I], the encoded q
+    (uint8 e4m3 codes or uint16 bf16 bits) with q_sf, the encoded k with k_sf, and k_row [n_q]."""
+    wl = inp["wl"]
+    keep = _Keep()
+    s = _Prolog()
+    s.n_q, s.B, s.d_q, s.d_model, s.H_I, s.d_I = wl.n_q, wl.B, wl.d_q, wl.d_model, wl.H_I, wl.d_I
+    mx = wl.li_dtype == "mxfp8"
+    s.mx = 1 if mx else 0
+    for k in ("xq", "x", "w_q", "w_k", "w_w", "ln_gamma", "ln_beta"):
+        setattr(s, k, keep.ptr(inp[k]))
+    s.ln_eps, s.w_scale = float(inp["ln_eps"]), float(inp["w_scale"])
+    s.page_table = keep.ptr(inp["pt_k"])
+    s.max_pages, s.page_size = int(inp["pt_k"].shape[1]), wl.page_size
+    s.seq_lens, s.q_start = keep.ptr(inp["seq_lens"]), keep.ptr(inp["q_start"])
+    n, F, D = wl.n_q, wl.H_I * wl.d_I, wl.d_I
+    r = {"q_val": np.zeros((n, F)), "k_val": np.zeros((n, D)), "w": np.zeros((n, wl.H_I)),
+         "q_enc": np.zeros((n, F), dtype=np.uint8 if mx else np.uint16),
+         "k_enc": np.zeros((n, D), dtype=np.uint8 if mx else np.uint16),
+         "q_sf": np.zeros((n, F // 32), dtype=np.uint8), "k_sf": np.zeros((n, D // 32), dtype=np.uint8),
+         "k_row": np.zeros(n, dtype=np.int64)}
+    f = lib().oracle_prolog
+    f.argtypes = [ctypes.c_void_p] * 9
+    rc = f(ctypes.byref(s), *(ctypes.c_void_p(r[k].ctypes.data) for k in
+                              ("q_val", "k_val", "w", "q_enc", "q_sf", "k_enc", "k_sf", "k_row")))
+    if rc != 0:
+        raise ValueError("oracle_prolog failed: %d" % rc)
+    return r
+
+
+def mx_quantize(v):
+    """OCP MX quantisation of a float64 vector (length a multiple of 32): (codes, scale bytes)."""
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    codes = np.zeros(v.shape[0], dtype=np.uint8)
+    sf = np.zeros(v.shape[0] // 32, dtype=np.uint8)
+    f = lib().oracle_mx_quantize
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    rc = f(v.ctypes.data, v.shape[0], codes.ctypes.data, sf.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_mx_quantize failed: %d" % rc)
+    return codes, sf
 
 
 def decode_bf16(bits: int) -> float:

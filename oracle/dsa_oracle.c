@@ -332,4 +332,169 @@ int oracle_sfa(const orc_sfa* S, int n_tok, const int* toks, const int* idx, dou
   return err;
 }
 
-int oracle_abi_version(void) { return 2; }
+/* ---- Indexer Prolog: the indexer's input preparation -------------------------------- */
+/*
+ * "Inference Optimization for Kimi K3.1 Pro", section 3 (Indexer Prolog) and section 5
+ * (three-stream prolog); "Day0 Inference Adaptation ... CANN", section 3.3 (the indexer fully
+ * quantised to MXFP8 with group size 32, projections kept in BF16).  For each new token t:
+ *   Q projection      q[t]   = W_q . xq[t]                 ([H_I*d_I], row f = h*d_I + d)
+ *   K normalisation   k[t]   = LayerNorm(W_k . x[t]) * gamma + beta   (over the d_I features)
+ *   head weights      w[t]   = w_scale * (W_w . x[t])       ([H_I])
+ *   quantisation      q[t] and k[t] to MXFP8 (OCP Microscaling rule, groups of 32 features) or
+ *                     to bf16 (round to nearest even); k[t] is written to the key cache at the
+ *                     token's position p_t: row pt[b][p_t / page_size] * page_size + p_t % page_size.
+ */
+
+/* Nearest e4m3 code to y (|y| clamped to 448 first), ties to the even code; from the format's
+ * value table (orc_e4m3), searched exhaustively. */
+static uint8_t orc_e4m3_encode(double y) {
+  int neg = y < 0.0;
+  double a = fabs(y);
+  if (a > 448.0) a = 448.0;
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < 127; ++c) { /* 0x00 .. 0x7E: every finite non-negative code */
+    double d = fabs(orc_e4m3((uint8_t)c) - a);
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  if (best == 0) return 0; /* +0 (a signed zero carries no information here) */
+  return (uint8_t)(best | (neg ? 0x80 : 0));
+}
+
+/* bf16 bits nearest to v: 8 significant bits, ties to even (rint in the default rounding mode),
+ * for v in bf16's normal range. */
+static uint16_t orc_bf16_encode(double v) {
+  if (v == 0.0) return signbit(v) ? 0x8000 : 0;
+  int e;
+  double m = frexp(v, &e);                   /* |m| in [0.5, 1) */
+  float f = (float)ldexp(rint(ldexp(m, 8)), e - 8); /* exactly representable */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+/* OCP Microscaling quantisation of n values (n a multiple of 32), group by group: shared exponent
+ * e = floor(log2(amax)) - 8 (8 = exponent of e4m3's largest normal), clamped to [-127, 127], 0 for
+ * an all-zero group; scale byte e + 127; codes = nearest e4m3 to v / 2^e. */
+int oracle_mx_quantize(const double* v, int n, uint8_t* codes, uint8_t* sf) {
+  if (!v || !codes || !sf || n < 0 || n % 32) return ORC_EARG;
+  for (int g = 0; g < n / 32; ++g) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i)
+      if (fabs(v[g * 32 + i]) > amax) amax = fabs(v[g * 32 + i]);
+    int e = 0;
+    if (amax > 0.0) {
+      int ex;
+      frexp(amax, &ex); /* amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1 */
+      e = ex - 1 - 8;
+      if (e < -127) e = -127;
+      if (e > 127) e = 127;
+    }
+    sf[g] = (uint8_t)(e + 127);
+    for (int i = 0; i < 32; ++i) codes[g * 32 + i] = orc_e4m3_encode(ldexp(v[g * 32 + i], -e));
+  }
+  return ORC_OK;
+}
+
+typedef struct {
+  int n_q, B, d_q, d_model, H_I, d_I;
+  int mx;                     /* 1: MXFP8 outputs; 0: bf16 outputs                     */
+  const uint16_t* xq;         /* [n_q][d_q] bf16, input of the Q projection              */
+  const uint16_t* x;          /* [n_q][d_model] bf16, input of the K and weight projections */
+  const uint16_t* w_q;        /* [H_I*d_I][d_q] bf16                                     */
+  const uint16_t* w_k;        /* [d_I][d_model] bf16                                     */
+  const uint16_t* w_w;        /* [H_I][d_model] bf16                                     */
+  const float* ln_gamma;      /* [d_I]                                                   */
+  const float* ln_beta;       /* [d_I]                                                   */
+  double ln_eps, w_scale;
+  const int* page_table;      /* [B][max_pages]                                          */
+  int max_pages, page_size;
+  const int* seq_lens;        /* [B]                                                     */
+  const int* q_start;         /* [B+1]                                                   */
+} orc_prolog;
+
+/* Fills, per token: q_val [n_q][H_I*d_I] and k_val [n_q][d_I] (fp64, before rounding),
+ * w_out [n_q][H_I]; the encoded q (q_enc: e4m3 codes or bf16 bits, q_sf) and k (k_enc, k_sf);
+ * k_row [n_q] = physical key-cache row of the token.  Any output pointer may be NULL. */
+int oracle_prolog(const orc_prolog* P, double* q_val, double* k_val, double* w_out, void* q_enc,
+                  uint8_t* q_sf, void* k_enc, uint8_t* k_sf, long long* k_row) {
+  if (!P || P->n_q < 0 || P->B <= 0 || P->d_q <= 0 || P->d_model <= 0 || P->H_I <= 0 ||
+      P->d_I <= 0 || P->d_I % 32 || !P->xq || !P->x || !P->w_q || !P->w_k || !P->w_w ||
+      !P->ln_gamma || !P->ln_beta || !P->page_table || !P->seq_lens || !P->q_start ||
+      P->page_size <= 0)
+    return ORC_EARG;
+  const int F = P->H_I * P->d_I;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int t = 0; t < P->n_q; ++t) {
+    double* q = (double*)malloc(sizeof(double) * (size_t)F);
+    double* k = (double*)malloc(sizeof(double) * (size_t)P->d_I);
+    uint8_t* c = (uint8_t*)malloc((size_t)F);
+    uint8_t* g = (uint8_t*)malloc((size_t)F / 32);
+    if (!q || !k || !c || !g) {
+      free(q); free(k); free(c); free(g);
+#pragma omp atomic write
+      err = ORC_ENOMEM;
+      continue;
+    }
+    for (int f = 0; f < F; ++f) {
+      double acc = 0.0;
+      for (int i = 0; i < P->d_q; ++i)
+        acc += orc_bf16(P->w_q[(long long)f * P->d_q + i]) * orc_bf16(P->xq[(long long)t * P->d_q + i]);
+      q[f] = acc;
+    }
+    for (int d = 0; d < P->d_I; ++d) {
+      double acc = 0.0;
+      for (int i = 0; i < P->d_model; ++i)
+        acc += orc_bf16(P->w_k[(long long)d * P->d_model + i]) * orc_bf16(P->x[(long long)t * P->d_model + i]);
+      k[d] = acc;
+    }
+    double mean = 0.0, var = 0.0;
+    for (int d = 0; d < P->d_I; ++d) mean += k[d];
+    mean /= P->d_I;
+    for (int d = 0; d < P->d_I; ++d) var += (k[d] - mean) * (k[d] - mean);
+    var /= P->d_I;
+    const double rstd = 1.0 / sqrt(var + P->ln_eps);
+    for (int d = 0; d < P->d_I; ++d)
+      k[d] = (k[d] - mean) * rstd * (double)P->ln_gamma[d] + (double)P->ln_beta[d];
+    if (w_out)
+      for (int h = 0; h < P->H_I; ++h) {
+        double acc = 0.0;
+        for (int i = 0; i < P->d_model; ++i)
+          acc += orc_bf16(P->w_w[(long long)h * P->d_model + i]) * orc_bf16(P->x[(long long)t * P->d_model + i]);
+        w_out[(long long)t * P->H_I + h] = P->w_scale * acc;
+      }
+    if (q_val) memcpy(q_val + (long long)t * F, q, sizeof(double) * (size_t)F);
+    if (k_val) memcpy(k_val + (long long)t * P->d_I, k, sizeof(double) * (size_t)P->d_I);
+    if (P->mx) {
+      oracle_mx_quantize(q, F, c, g);
+      if (q_enc) memcpy((uint8_t*)q_enc + (long long)t * F, c, (size_t)F);
+      if (q_sf) memcpy(q_sf + (long long)t * F / 32, g, (size_t)F / 32);
+      oracle_mx_quantize(k, P->d_I, c, g);
+      if (k_enc) memcpy((uint8_t*)k_enc + (long long)t * P->d_I, c, (size_t)P->d_I);
+      if (k_sf) memcpy(k_sf + (long long)t * P->d_I / 32, g, (size_t)P->d_I / 32);
+    } else {
+      if (q_enc)
+        for (int f = 0; f < F; ++f) ((uint16_t*)q_enc)[(long long)t * F + f] = orc_bf16_encode(q[f]);
+      if (k_enc)
+        for (int d = 0; d < P->d_I; ++d)
+          ((uint16_t*)k_enc)[(long long)t * P->d_I + d] = orc_bf16_encode(k[d]);
+    }
+    if (k_row) {
+      int b, p;
+      if (locate(P->q_start, P->seq_lens, P->B, t, &b, &p) ||
+          p / P->page_size >= P->max_pages) {
+        k_row[t] = -1;
+      } else {
+        k_row[t] = phys_row(P->page_table, P->max_pages, P->page_size, b, p);
+      }
+    }
+    free(q); free(k); free(c); free(g);
+  }
+  return err;
+}
+
+int oracle_abi_version(void) { return 3; }

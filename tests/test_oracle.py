@@ -299,6 +299,99 @@ def test_mx_generator_quantiser_follows_the_format():
     assert torch.all((codes - scaled).abs()[normal] <= scaled.abs()[normal] * 2.0 ** -4)
 
 
+# ---------------------------------------------------------------- Indexer Prolog
+
+@pytest.mark.parametrize("case", range(4))
+def test_mx_quantiser_hand_cases(case):
+    c = _gold("mx_quant_hand_cases.json")["cases"][case]
+    v = np.zeros(32)
+    v[:len(c["values"])] = c["values"]
+    codes, sf = oracle.mx_quantize(v)
+    assert sf.tolist() == [c["sf"]]
+    assert codes[:len(c["codes"])].tolist() == c["codes"]
+    assert not codes[len(c["codes"]):].any()
+
+
+def test_mx_quantiser_rounding_matches_torch_e4m3_conversion():
+    """Element rounding against torch's float8_e4m3fn conversion (round to nearest even) of the
+    values divided by the group scale, over groups spanning 2^-20 .. 2^20 in magnitude."""
+    g = np.random.default_rng(4)
+    v = g.standard_normal(32 * 64) * np.repeat(2.0 ** g.integers(-20, 21, 64), 32)
+    codes, sf = oracle.mx_quantize(v)
+    scale = np.repeat(np.ldexp(1.0, sf.astype(np.int64) - 127), 32)
+    y = torch.tensor(v / scale).clamp(-448, 448)
+    ref = y.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()  # v/scale exact in fp32
+    ref = np.where(ref == 0x80, 0, ref)  # -0 -> +0, as the quantiser emits
+    assert np.array_equal(codes, ref)
+    amax = np.abs(v).reshape(64, 32).max(1)
+    assert np.all((amax / np.ldexp(1.0, sf.astype(np.int64) - 127) >= 256) &
+                  (amax / np.ldexp(1.0, sf.astype(np.int64) - 127) < 512))
+
+
+def _prolog_small(values="normal", li_dtype="mxfp8", **over):
+    kw = dict(seq_lens=[300, 130, 65], n_new=[1, 2, 3], d_q=64, d_model=96, values=values,
+              li_dtype=li_dtype)
+    kw.update(over)
+    wl = di.small("prolog_decode_32k", **kw)
+    return di.generate_prolog(wl)
+
+
+@pytest.mark.parametrize("values", ["int4", "normal"])
+def test_prolog_projections_match_library_matmul(values):
+    inp = _prolog_small(values)
+    r = oracle.prolog(inp)
+    q = (inp["xq"].double() @ inp["w_q"].double().T).numpy()
+    w = inp["w_scale"] * (inp["x"].double() @ inp["w_w"].double().T).numpy()
+    if values == "int4":
+        assert np.array_equal(r["q_val"], q) and np.array_equal(r["w"], w)
+    else:
+        np.testing.assert_allclose(r["q_val"], q, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(r["w"], w, rtol=1e-12, atol=1e-14)
+
+
+def test_prolog_layernorm_matches_torch():
+    inp = _prolog_small()
+    r = oracle.prolog(inp)
+    z = inp["x"].double() @ inp["w_k"].double().T
+    ref = torch.nn.functional.layer_norm(z, (z.shape[1],), inp["ln_gamma"].double(),
+                                         inp["ln_beta"].double(), eps=inp["ln_eps"])
+    np.testing.assert_allclose(r["k_val"], ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_prolog_layernorm_closed_forms():
+    """Identical K-projection rows make every feature equal: the normalised key is beta.  With
+    eps = 0, scaling the activations leaves the normalised key unchanged."""
+    inp = _prolog_small()
+    same = dict(inp, w_k=inp["w_k"][:1].expand_as(inp["w_k"]).contiguous())
+    r = oracle.prolog(same)
+    np.testing.assert_allclose(r["k_val"], np.broadcast_to(inp["ln_beta"].double().numpy(),
+                                                           r["k_val"].shape), atol=1e-12)
+    a = oracle.prolog(dict(inp, ln_eps=0.0))
+    b = oracle.prolog(dict(inp, ln_eps=0.0, x=(inp["x"].float() * 4).to(torch.bfloat16)))
+    np.testing.assert_allclose(a["k_val"], b["k_val"], rtol=1e-12, atol=1e-12)
+
+
+def test_prolog_encodings_and_cache_rows():
+    """MX outputs are the pinned quantiser applied per head / per key; bf16 outputs on
+    integer inputs are the exact values; each token's key goes to its position's row."""
+    inp = _prolog_small()
+    wl = inp["wl"]
+    r = oracle.prolog(inp)
+    for t in range(wl.n_q):
+        c, s = oracle.mx_quantize(r["q_val"][t])
+        assert np.array_equal(c, r["q_enc"][t]) and np.array_equal(s, r["q_sf"][t])
+        c, s = oracle.mx_quantize(r["k_val"][t])
+        assert np.array_equal(c, r["k_enc"][t]) and np.array_equal(s, r["k_sf"][t])
+    pos = di.token_positions(wl)
+    seq = [b for b, n in enumerate(wl.n_new) for _ in range(n)]
+    pt = inp["pt_k"]
+    assert r["k_row"].tolist() == [int(pt[b, p // 64]) * 64 + p % 64 for b, p in zip(seq, pos)]
+    ib = _prolog_small("int4", li_dtype="bf16")
+    rb = oracle.prolog(ib)
+    qb = torch.tensor(rb["q_val"]).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    assert np.array_equal(rb["q_enc"], qb)  # integers below 2^8 are exact in bf16
+
+
 # ---------------------------------------------------------------- top-K: definition by brute force
 
 def _check_selection(s, idx_row, cnt, K):
