@@ -32,7 +32,7 @@ DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
 SYMBOLS = ["dsa_status_string", "dsa_last_error", "dsa_abi_version", "dsa_li_topk",
            "dsa_sfa_workspace_bytes", "dsa_sfa_decode", "dsa_sfa_prefill",
            "dsa_sfa_decode_static", "dsa_page_bytes", "dsa_page_table_validate",
-           "dsa_cache_write"]
+           "dsa_cache_write", "dsa_prolog_workspace_bytes", "dsa_indexer_prolog"]
 
 # Capacity of the library's fixed scratch array used by dsa_sfa_decode_static.
 SFA_STATIC_SCRATCH_BYTES = 20 * 1024 * 1024
@@ -51,6 +51,16 @@ class LiArgs(ctypes.Structure):
         "max_q_per_seq", "dtype")] + [(n, ctypes.c_void_p) for n in (
             "q", "q_scale", "w", "k_pool", "k_scale", "page_table", "seq_lens", "q_start",
             "out_idx", "out_cnt", "status", "q_sf", "k_sf")]
+
+
+class PrologArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "n_q", "B", "d_q", "d_model", "H_I", "d_I", "dtype", "page_size", "max_pages",
+        "num_pages")] + [("ln_eps", ctypes.c_float), ("w_scale", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in (
+            "xq", "x", "w_q", "w_k", "w_w", "ln_gamma", "ln_beta", "page_table", "seq_lens",
+            "q_start", "q_out", "q_sf", "w_out", "k_pool", "k_sf", "workspace")] + [
+        ("workspace_bytes", ctypes.c_size_t), ("status", ctypes.c_void_p)]
 
 
 class SfaArgs(ctypes.Structure):
@@ -91,6 +101,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.dsa_page_table_validate.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int]
     lib.dsa_page_table_validate.restype = ctypes.c_int
+    lib.dsa_prolog_workspace_bytes.argtypes = [ctypes.POINTER(PrologArgs)]
+    lib.dsa_prolog_workspace_bytes.restype = ctypes.c_size_t
+    lib.dsa_indexer_prolog.argtypes = [ctypes.POINTER(PrologArgs), P]
+    lib.dsa_indexer_prolog.restype = ctypes.c_int
     lib.dsa_cache_write.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     P, ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_int, P, P]
     lib.dsa_cache_write.restype = ctypes.c_int
@@ -276,6 +290,58 @@ def cache_write(pool, page_table, seq, pos, rows, *, scale_pool=None, row_scales
                                page_table.shape[0], _ptr(seq), _ptr(pos), _ptr(rows),
                                _ptr(row_scales), rows.shape[0], _ptr(status), _stream(stream))
     _check(code, "dsa_cache_write")
+
+
+def prolog_args(inp: dict, *, q_out, q_sf, w_out, workspace=None, status=None):
+    """Fill the C argument struct of dsa_indexer_prolog from a ``dsa_inputs.generate_prolog``
+    dict (device tensors; the key cache in it is written in place)."""
+    wl = inp["wl"]
+    a = PrologArgs()
+    a.n_q, a.B, a.d_q, a.d_model = inp["xq"].shape[0], inp["seq_lens"].shape[0], \
+        inp["xq"].shape[1], inp["x"].shape[1]
+    a.H_I, a.d_I = inp["w_w"].shape[0], inp["w_k"].shape[0]
+    a.dtype = DSA_MXFP8_E4M3 if inp.get("k_sf") is not None else DSA_BF16
+    a.page_size, a.max_pages, a.num_pages = inp["k_pool"].shape[1], inp["pt_k"].shape[1], \
+        inp["k_pool"].shape[0]
+    a.ln_eps, a.w_scale = float(inp["ln_eps"]), float(inp["w_scale"])
+    for k in ("xq", "x", "w_q", "w_k", "w_w", "ln_gamma", "ln_beta", "seq_lens", "q_start",
+              "k_pool", "k_sf"):
+        setattr(a, k, _ptr(inp.get(k)))
+    a.page_table = _ptr(inp["pt_k"])
+    a.q_out, a.q_sf, a.w_out = _ptr(q_out), _ptr(q_sf), _ptr(w_out)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a.status = _ptr(status)
+    del wl
+    return a
+
+
+def prolog_workspace_bytes(inp: dict) -> int:
+    a = prolog_args(inp, q_out=None, q_sf=None, w_out=None)
+    return int(load().dsa_prolog_workspace_bytes(ctypes.byref(a)))
+
+
+def indexer_prolog(inp: dict, *, q_out=None, q_sf=None, w_out=None, workspace=None, status=None,
+                   stream=None):
+    """Indexer Prolog of the new tokens: returns (q, q_sf or None, w) and writes the new keys into
+    inp["k_pool"] (and inp["k_sf"]).  ``workspace``: a zeroed uint8 device tensor of
+    prolog_workspace_bytes(inp) bytes (allocated here when not given)."""
+    lib = load()
+    n_q, H_I, d_I = inp["xq"].shape[0], inp["w_w"].shape[0], inp["w_k"].shape[0]
+    dev = inp["xq"].device
+    mx = inp.get("k_sf") is not None
+    if q_out is None:
+        q_out = torch.empty((n_q, H_I, d_I), dtype=torch.float8_e4m3fn if mx else torch.bfloat16,
+                            device=dev)
+    if q_sf is None and mx:
+        q_sf = torch.empty((n_q, H_I, d_I // 32), dtype=torch.uint8, device=dev)
+    if w_out is None:
+        w_out = torch.empty((n_q, H_I), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.zeros(max(prolog_workspace_bytes(inp), 256), dtype=torch.uint8, device=dev)
+    a = prolog_args(inp, q_out=q_out, q_sf=q_sf, w_out=w_out, workspace=workspace, status=status)
+    _check(lib.dsa_indexer_prolog(ctypes.byref(a), _stream(stream)), "dsa_indexer_prolog")
+    return q_out, q_sf, w_out
 
 
 def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=None, status=None,

@@ -213,6 +213,43 @@ dsa_status dsa_sfa_prefill(const dsa_sfa_args* a, dsa_stream_t stream) {
   return sfa_common(a, true, stream);
 }
 
+static dsa_status prolog_check(const dsa_prolog_args* a, bool pointers) {
+  if (!a) return fail(DSA_ERR_INVALID_ARG, "indexer_prolog: null args");
+  if (a->n_q < 0 || a->B <= 0 || a->d_q <= 0 || a->d_model <= 0 || a->max_pages <= 0 ||
+      a->num_pages <= 0)
+    return fail(DSA_ERR_INVALID_ARG, "indexer_prolog: non-positive size");
+  if (a->H_I != 64 || a->d_I != 128 || a->page_size != 64)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer_prolog: needs H_I 64, d_I 128, page_size 64");
+  if (a->dtype != DSA_MXFP8_E4M3 && a->dtype != DSA_BF16)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer_prolog: dtype must be MXFP8_E4M3 or BF16");
+  if (a->d_q % 8 || a->d_model % 8)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer_prolog: d_q and d_model must be multiples of 8");
+  if (!pointers) return DSA_OK;  // sizes only (workspace query)
+  if (!a->xq || !a->x || !a->w_q || !a->w_k || !a->w_w || !a->ln_gamma || !a->ln_beta ||
+      !a->page_table || !a->seq_lens || !a->q_start || !a->q_out || !a->w_out || !a->k_pool ||
+      !a->workspace || (a->dtype == DSA_MXFP8_E4M3 && (!a->q_sf || !a->k_sf)))
+    return fail(DSA_ERR_INVALID_ARG, "indexer_prolog: null device pointer");
+  if (!aligned16(a->xq) || !aligned16(a->x) || !aligned16(a->w_q) || !aligned16(a->w_k) ||
+      !aligned16(a->w_w))
+    return fail(DSA_ERR_INVALID_ARG, "indexer_prolog: inputs and weights must be 16-byte aligned");
+  return DSA_OK;
+}
+
+size_t dsa_prolog_workspace_bytes(const dsa_prolog_args* a) {
+  if (prolog_check(a, false) != DSA_OK) return 0;
+  return dsa::prolog_workspace_bytes(*a);
+}
+
+dsa_status dsa_indexer_prolog(const dsa_prolog_args* a, dsa_stream_t stream) {
+  g_last_error.clear();
+  const dsa_status c = prolog_check(a, true);
+  if (c != DSA_OK) return c;
+  std::string err;
+  const dsa_status s = dsa::launch_prolog(*a, reinterpret_cast<cudaStream_t>(stream), err);
+  if (s != DSA_OK) g_last_error = err;
+  return s;
+}
+
 dsa_status dsa_cache_write(void* pool, float* scale_pool, int num_pages, int page_size, int dim,
                            int elem_bytes, const int32_t* page_table, int max_pages, int B,
                            const int32_t* seq, const int32_t* pos, const void* rows,

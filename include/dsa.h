@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -190,6 +190,66 @@ dsa_status dsa_sfa_prefill(const dsa_sfa_args* args, dsa_stream_t stream);
  */
 #define DSA_SFA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
 dsa_status dsa_sfa_decode_static(const dsa_sfa_args* args, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Indexer Prolog                                                                              */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * The indexer's input preparation for the new tokens ("Inference Optimization for Kimi K3.1 Pro",
+ * section 3, Indexer Prolog, and section 4, MXFP8 indexer path; "Day0 Inference Adaptation ...
+ * CANN", section 3.3).  For each new token t (sequence b, position p = seq_lens[b] - n_b + i):
+ *   q[t][h][:] = W_q[h*d_I .. h*d_I+d_I) . xq[t]                 -> q_out (+ q_sf)
+ *   k[t]       = LayerNorm(W_k . x[t]) * ln_gamma + ln_beta        -> key-cache row of p
+ *   w[t][h]    = w_scale * (W_w[h] . x[t])                         -> w_out (fp32)
+ * LayerNorm: mean and biased variance over the d_I features, then (v - mean) / sqrt(var + eps).
+ * dtype DSA_MXFP8_E4M3: q and k become e4m3 codes with one E8M0 scale byte per 32 features
+ * (shared exponent floor(log2(max |v|)) - 8, clamped to [-127, 127], 0 for an all-zero group;
+ * elements v / 2^e rounded to nearest even, saturated at 448; a zero is +0) -- the layout
+ * dsa_li_topk reads in its MXFP8 mode; dtype DSA_BF16: bf16, round to nearest even.
+ * The three projections run as concurrent CTA roles of one launch (no stream fork).
+ *
+ * Supported: H_I = 64, d_I = 128, page_size 64; d_q and d_model multiples of 8; bf16 inputs and
+ * weights, 16-byte aligned.  A position whose page id is outside [0, num_pages) sets
+ * DSA_ERR_DEVICE_CHECK and its key row is not written.
+ */
+typedef struct {
+  int n_q;              /* new tokens (= q_start[B])                                       */
+  int B;
+  int d_q;              /* input width of the Q projection                                 */
+  int d_model;          /* input width of the K and head-weight projections                */
+  int H_I, d_I;         /* 64, 128                                                         */
+  dsa_dtype dtype;      /* DSA_MXFP8_E4M3 or DSA_BF16: format of q_out and of the key cache */
+  int page_size;        /* 64                                                              */
+  int max_pages;        /* row stride of page_table                                        */
+  int num_pages;        /* pages in k_pool                                                 */
+  float ln_eps;
+  float w_scale;        /* head-weight scale                                               */
+  const void* xq;       /* [n_q][d_q] bf16                                                 */
+  const void* x;        /* [n_q][d_model] bf16                                             */
+  const void* w_q;      /* [H_I*d_I][d_q] bf16                                             */
+  const void* w_k;      /* [d_I][d_model] bf16                                             */
+  const void* w_w;      /* [H_I][d_model] bf16                                             */
+  const float* ln_gamma;/* [d_I]                                                           */
+  const float* ln_beta; /* [d_I]                                                           */
+  const int32_t* page_table; /* [B][max_pages] of the key cache                           */
+  const int32_t* seq_lens;   /* [B] positions, new tokens included                        */
+  const int32_t* q_start;    /* [B+1]                                                     */
+  void* q_out;          /* [n_q][H_I][d_I] e4m3 codes or bf16                              */
+  uint8_t* q_sf;        /* [n_q][H_I][d_I/32] (MXFP8)                                      */
+  float* w_out;         /* [n_q][H_I]                                                      */
+  void* k_pool;         /* [num_pages][page_size][d_I] e4m3 codes or bf16 (written rows only) */
+  uint8_t* k_sf;        /* [num_pages][page_size][d_I/32] (MXFP8)                          */
+  void* workspace;      /* dsa_prolog_workspace_bytes() bytes, zeroed once before first use;
+                           a call leaves its counters at zero again (not after a timeout)  */
+  size_t workspace_bytes;
+  int32_t* status;      /* device int32 error word, or NULL                                */
+} dsa_prolog_args;
+
+/* Scratch bytes dsa_indexer_prolog needs for these sizes on the current device (only the size
+ * fields are read; 0 if they are invalid). */
+size_t dsa_prolog_workspace_bytes(const dsa_prolog_args* args);
+dsa_status dsa_indexer_prolog(const dsa_prolog_args* args, dsa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* Cache layout and page-table helpers                                                         */

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     lib = dsa.load()
-    assert lib.dsa_abi_version() == 2
+    assert lib.dsa_abi_version() == 3
     assert dsa.status_string(0) == "DSA_OK"
     assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
     assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"
@@ -39,6 +39,7 @@ def test_struct_layouts_match_header():
     """ctypes mirrors of the argument structs have the C sizes (x86_64 / aarch64 LP64)."""
     assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 13 * 8
     assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8
+    assert ctypes.sizeof(dsa.PrologArgs) == 10 * 4 + 2 * 4 + 16 * 8 + 8 + 8
 
 
 def test_page_bytes():
@@ -131,3 +132,36 @@ def test_cache_write_host_validation():
     assert lib.dsa_cache_write(P, None, 4, 64, 4, 2, P, 4, 1, P, P, P, None, 1, None, None) == dsa.DSA_ERR_UNSUPPORTED
     assert lib.dsa_cache_write(P, P, 4, 64, 576, 2, P, 4, 1, P, P, P, None, 1, None, None) == dsa.DSA_ERR_INVALID_ARG
     assert lib.dsa_cache_write(P, None, 4, 64, 576, 2, P, 4, 1, P, P, P, None, 0, None, None) == dsa.DSA_OK
+
+
+def _prolog(**over):
+    a = dsa.PrologArgs()
+    a.n_q, a.B, a.d_q, a.d_model, a.H_I, a.d_I = 4, 2, 1536, 7168, 64, 128
+    a.dtype, a.page_size, a.max_pages, a.num_pages = dsa.DSA_MXFP8_E4M3, 64, 8, 16
+    a.ln_eps, a.w_scale = 1e-6, 0.125
+    for n in ("xq", "x", "w_q", "w_k", "w_w", "ln_gamma", "ln_beta", "page_table", "seq_lens",
+              "q_start", "q_out", "q_sf", "w_out", "k_pool", "k_sf", "workspace"):
+        setattr(a, n, 4096)  # fake, aligned, never dereferenced on these error paths
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    ({"B": 0}, dsa.DSA_ERR_INVALID_ARG),
+    ({"n_q": -1}, dsa.DSA_ERR_INVALID_ARG),
+    ({"H_I": 32}, dsa.DSA_ERR_UNSUPPORTED),
+    ({"d_I": 64}, dsa.DSA_ERR_UNSUPPORTED),
+    ({"dtype": dsa.DSA_FP8_E4M3}, dsa.DSA_ERR_UNSUPPORTED),   # per-token FP8 is not produced
+    ({"d_q": 1540}, dsa.DSA_ERR_UNSUPPORTED),                 # row stride not a multiple of 16 B
+    ({"k_sf": None}, dsa.DSA_ERR_INVALID_ARG),                # MXFP8 needs the scale arrays
+    ({"x": 4100}, dsa.DSA_ERR_INVALID_ARG),                   # misaligned
+])
+def test_indexer_prolog_host_validation(over, code):
+    lib = dsa.load()
+    a = _prolog(**over)
+    assert lib.dsa_indexer_prolog(ctypes.byref(a), None) == code
+    assert dsa.last_error()
+    if code == dsa.DSA_ERR_UNSUPPORTED or over.get("B") == 0 or "n_q" in over:
+        assert lib.dsa_prolog_workspace_bytes(ctypes.byref(a)) == 0
+    assert lib.dsa_indexer_prolog(None, None) == dsa.DSA_ERR_INVALID_ARG
