@@ -450,9 +450,111 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_prolog(args):
+    """The Indexer Prolog alone (workload prolog_*): per-launch CUDA-event times with an L2 flush
+    between launches (the prolog's weights fit in L2; in a model, other layers evict them)."""
+    import torch
+    import dsa_inputs as di
+    import dsa_sparse_attention_li_gb300 as dsa
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = di.preset(args.workload)
+    if world > 1:
+        wl = di.Workload(**{**wl.__dict__, "seed": wl.seed + 100 * rank})
+    inp = di.generate_prolog(wl, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_q, F = wl.n_q, wl.H_I * wl.d_I
+    mx = wl.li_dtype == "mxfp8"
+    q = torch.empty((n_q, wl.H_I, wl.d_I), dtype=torch.float8_e4m3fn if mx else torch.bfloat16, device=dev)
+    qsf = torch.empty((n_q, wl.H_I, wl.d_I // 32), dtype=torch.uint8, device=dev) if mx else None
+    w = torch.empty((n_q, wl.H_I), dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(dsa.prolog_workspace_bytes(inp), 256), dtype=torch.uint8, device=dev)
+    lib = dsa.load()
+    a = dsa.prolog_args(inp, q_out=q, q_sf=qsf, w_out=w, workspace=ws, status=status)
+    stream = torch.cuda.Stream(device=dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 2x the 129 MB L2
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            if lib.dsa_indexer_prolog(ctypes.byref(a), sp):
+                raise RuntimeError("prolog launch failed: " + dsa.last_error())
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(status.item()))
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(None) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush.zero_()
+                ev[i][0].record(stream)
+                lib.dsa_indexer_prolog(ctypes.byref(a), sp)
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the timed region" % int(status.item()))
+    us = statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1000.0
+    t = torch.tensor([us], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    us = float(t.item())
+    if rank != 0:
+        return
+    # algorithmic bytes: weights once, activations once, quantised q, head weights, key rows
+    w_bytes = (F * wl.d_q + wl.d_I * wl.d_model + wl.H_I * wl.d_model) * 2
+    a_bytes = n_q * (wl.d_q + wl.d_model) * 2
+    o_bytes = n_q * (F * (1 + 1 / 32) if mx else F * 2) + n_q * wl.H_I * 4 + \
+        n_q * (wl.d_I * (1 + 1 / 32) if mx else wl.d_I * 2)
+    bytes_ = w_bytes + a_bytes + o_bytes
+    flop = 2 * n_q * (F * wl.d_q + (wl.d_I + wl.H_I) * wl.d_model)
+    hbm, _, peak_kind = measured_peaks()
+    gbs = bytes_ / (us * 1e-6) / 1e9
+    line = {
+        "metric": "indexer_prolog_tokens_per_s", "value": n_q * world / (us * 1e-6), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": us / 1000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.li_dtype,
+        "data": "synthetic",
+        "config": {"workload": wl.name, "n_q": n_q, "d_q": wl.d_q, "d_model": wl.d_model,
+                   "H_I": wl.H_I, "d_I": wl.d_I, "seed": wl.seed,
+                   "l2": "L2 flushed (256 MB write) before every timed launch; per-launch CUDA events",
+                   "launch": "one C-ABI launch per step (three CTA roles)"},
+        "roofline": {"kernel": "prolog", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": gbs / hbm, "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes": bytes_},
+        "kernels": {"prolog_us": us, "prolog_tflops": flop / (us * 1e-6) / 1e12},
+        "gpu_launches": K, "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        cpu = di.to_device(inp, "cpu")
+        sub = di.Workload(**{**wl.__dict__, "seq_lens": wl.seq_lens[:2], "n_new": wl.n_new[:2]})
+        sample = {k: v for k, v in cpu.items()}
+        sample.update(wl=sub, xq=cpu["xq"][:sum(sub.n_new)], x=cpu["x"][:sum(sub.n_new)],
+                      seq_lens=cpu["seq_lens"][:2], q_start=cpu["q_start"][:3],
+                      pt_k=cpu["pt_k"][:2])
+        t0 = time.time()
+        oracle.prolog(sample)
+        dt = time.time() - t0
+        line["cpu_baseline"] = {"value": sub.n_q / dt, "unit": "tokens/s",
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": "%d tokens of the workload" % sub.n_q}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.workload.startswith("prolog"):
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm times the decode path; the prolog has its own "
+                              "cpu_baseline"}))
+            return
+        run_prolog(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
