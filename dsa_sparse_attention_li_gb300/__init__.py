@@ -32,7 +32,7 @@ DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
 SYMBOLS = ["dsa_status_string", "dsa_last_error", "dsa_abi_version", "dsa_li_topk",
            "dsa_sfa_workspace_bytes", "dsa_sfa_decode", "dsa_sfa_prefill",
            "dsa_sfa_decode_static", "dsa_page_bytes", "dsa_page_table_validate",
-           "dsa_cache_write", "dsa_prolog_workspace_bytes", "dsa_indexer_prolog"]
+           "dsa_cache_write", "dsa_prolog_workspace_bytes", "dsa_indexer_prolog", "dsa_topk_merge"]
 
 # Capacity of the library's fixed scratch array used by dsa_sfa_decode_static.
 SFA_STATIC_SCRATCH_BYTES = 20 * 1024 * 1024
@@ -50,7 +50,12 @@ class LiArgs(ctypes.Structure):
         "B", "n_q", "H_I", "d_I", "K", "page_size", "max_pages", "num_pages", "max_seq_len",
         "max_q_per_seq", "dtype")] + [(n, ctypes.c_void_p) for n in (
             "q", "q_scale", "w", "k_pool", "k_scale", "page_table", "seq_lens", "q_start",
-            "out_idx", "out_cnt", "status", "q_sf", "k_sf")]
+            "out_idx", "out_cnt", "status", "q_sf", "k_sf", "out_score")]
+
+
+class MergeArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("S", "n_q", "K_in", "K")] + [
+        (n, ctypes.c_void_p) for n in ("cand_idx", "cand_score", "shard_offset", "out_idx", "out_cnt")]
 
 
 class PrologArgs(ctypes.Structure):
@@ -101,6 +106,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.dsa_page_table_validate.argtypes = [P, ctypes.c_int, ctypes.c_int, P, ctypes.c_int,
                                             ctypes.c_int, ctypes.c_int]
     lib.dsa_page_table_validate.restype = ctypes.c_int
+    lib.dsa_topk_merge.argtypes = [ctypes.POINTER(MergeArgs), P]
+    lib.dsa_topk_merge.restype = ctypes.c_int
     lib.dsa_prolog_workspace_bytes.argtypes = [ctypes.POINTER(PrologArgs)]
     lib.dsa_prolog_workspace_bytes.restype = ctypes.c_size_t
     lib.dsa_indexer_prolog.argtypes = [ctypes.POINTER(PrologArgs), P]
@@ -149,7 +156,7 @@ def _host_max(seq_lens: torch.Tensor, q_start: torch.Tensor, max_seq_len, max_q_
 
 def li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_scale=None,
                  max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None,
-                 q_sf=None, k_sf=None):
+                 q_sf=None, k_sf=None, out_score=None):
     """Fill the C argument struct of dsa_li_topk (tensors must outlive the call).  e4m3 q/k take
     either fp32 q_scale/k_scale (FP8) or uint8 E8M0 group scales q_sf/k_sf (MXFP8)."""
     fp8 = q.dtype == torch.float8_e4m3fn
@@ -167,13 +174,15 @@ def li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None
     a.page_table, a.seq_lens, a.q_start = _ptr(page_table), _ptr(seq_lens), _ptr(q_start)
     a.out_idx, a.out_cnt, a.status = _ptr(out_idx), _ptr(out_cnt), _ptr(status)
     a.q_sf, a.k_sf = _ptr(q_sf), _ptr(k_sf)
+    a.out_score = _ptr(out_score)
     return a
 
 
 def li_topk(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_scale=None,
             max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None,
-            stream=None, q_sf=None, k_sf=None):
-    """Fused indexer scoring + top-K.  Returns (idx [n_q, K] int32, cnt [n_q] int32)."""
+            stream=None, q_sf=None, k_sf=None, out_score=None):
+    """Fused indexer scoring + top-K.  Returns (idx [n_q, K] int32, cnt [n_q] int32); with
+    ``out_score`` ([n_q, K] fp32) also the score of every selected position."""
     lib = load()
     n_q = q.shape[0]
     if out_idx is None:
@@ -182,7 +191,8 @@ def li_topk(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_s
         out_cnt = torch.empty((n_q,), dtype=torch.int32, device=q.device)
     a = li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, q_scale=q_scale,
                      k_scale=k_scale, max_seq_len=max_seq_len, max_q_per_seq=max_q_per_seq,
-                     out_idx=out_idx, out_cnt=out_cnt, status=status, q_sf=q_sf, k_sf=k_sf)
+                     out_idx=out_idx, out_cnt=out_cnt, status=status, q_sf=q_sf, k_sf=k_sf,
+                     out_score=out_score)
     _check(lib.dsa_li_topk(ctypes.byref(a), _stream(stream)), "dsa_li_topk")
     return out_idx, out_cnt
 
@@ -290,6 +300,25 @@ def cache_write(pool, page_table, seq, pos, rows, *, scale_pool=None, row_scales
                                page_table.shape[0], _ptr(seq), _ptr(pos), _ptr(rows),
                                _ptr(row_scales), rows.shape[0], _ptr(status), _stream(stream))
     _check(code, "dsa_cache_write")
+
+
+def topk_merge(cand_idx, cand_score, shard_offset, K, *, out_idx=None, out_cnt=None, stream=None):
+    """Merge S shards' candidates ([S, n_q, K_in] shard-local positions and scores; position +
+    shard_offset[s] is the sequence position) into the top-K by (score desc, position asc),
+    ascending positions with -1 padding.  Returns (idx [n_q, K], cnt [n_q])."""
+    lib = load()
+    S, n_q, K_in = cand_idx.shape
+    dev = cand_idx.device
+    if out_idx is None:
+        out_idx = torch.empty((n_q, K), dtype=torch.int32, device=dev)
+    if out_cnt is None:
+        out_cnt = torch.empty((n_q,), dtype=torch.int32, device=dev)
+    a = MergeArgs()
+    a.S, a.n_q, a.K_in, a.K = S, n_q, K_in, int(K)
+    a.cand_idx, a.cand_score, a.shard_offset = _ptr(cand_idx), _ptr(cand_score), _ptr(shard_offset)
+    a.out_idx, a.out_cnt = _ptr(out_idx), _ptr(out_cnt)
+    _check(lib.dsa_topk_merge(ctypes.byref(a), _stream(stream)), "dsa_topk_merge")
+    return out_idx, out_cnt
 
 
 def prolog_args(inp: dict, *, q_out, q_sf, w_out, workspace=None, status=None):

@@ -213,6 +213,21 @@ dsa_status dsa_sfa_prefill(const dsa_sfa_args* a, dsa_stream_t stream) {
   return sfa_common(a, true, stream);
 }
 
+dsa_status dsa_topk_merge(const dsa_topk_merge_args* a, dsa_stream_t stream) {
+  g_last_error.clear();
+  if (!a) return fail(DSA_ERR_INVALID_ARG, "topk_merge: null args");
+  if (a->S <= 0 || a->n_q < 0 || a->K_in <= 0 || a->K <= 0)
+    return fail(DSA_ERR_INVALID_ARG, "topk_merge: non-positive size");
+  if ((long long)a->S * a->K_in > 16384 || a->K > 16384)
+    return fail(DSA_ERR_UNSUPPORTED, "topk_merge: S * K_in and K must be at most 16384");
+  if (a->n_q > 0 && (!a->cand_idx || !a->cand_score || !a->shard_offset || !a->out_idx))
+    return fail(DSA_ERR_INVALID_ARG, "topk_merge: null device pointer");
+  std::string err;
+  const dsa_status s = dsa::launch_topk_merge(*a, reinterpret_cast<cudaStream_t>(stream), err);
+  if (s != DSA_OK) g_last_error = err;
+  return s;
+}
+
 static dsa_status prolog_check(const dsa_prolog_args* a, bool pointers) {
   if (!a) return fail(DSA_ERR_INVALID_ARG, "indexer_prolog: null args");
   if (a->n_q < 0 || a->B <= 0 || a->d_q <= 0 || a->d_model <= 0 || a->max_pages <= 0 ||

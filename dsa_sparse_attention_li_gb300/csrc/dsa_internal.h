@@ -15,6 +15,7 @@ dsa_status launch_li_topk(const dsa_li_args& a, cudaStream_t stream, std::string
 dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, std::string& err);
 size_t sfa_workspace_bytes(const dsa_sfa_args& a);
 dsa_status launch_prolog(const dsa_prolog_args& a, cudaStream_t stream, std::string& err);
+dsa_status launch_topk_merge(const dsa_topk_merge_args& a, cudaStream_t stream, std::string& err);
 size_t prolog_workspace_bytes(const dsa_prolog_args& a);
 dsa_status launch_cache_write(void* pool, float* scale_pool, int num_pages, int page_size, int dim,
                               int elem_bytes, const int32_t* page_table, int max_pages, int B,

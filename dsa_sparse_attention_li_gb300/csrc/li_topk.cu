@@ -67,6 +67,7 @@ struct Params {
   const void* k_pool;
   const uint8_t* q_sf;  // MXFP8: E8M0 scales of 32-element groups, [n_q][H_I][D_I/32]
   const uint8_t* k_sf;  //        and [num_pages][64][D_I/32]
+  float* out_score;     // optional [n_q][K]: the score of every emitted position (-inf padding)
 };
 
 template <int D_I, bool FP8, int H_I, int T, bool MX = false>
@@ -1074,7 +1075,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          if ((take >> (4 * g + k)) & 1u) sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
+          if ((take >> (4 * g + k)) & 1u) {
+            if (p.out_score && off + (slot - e_lo) < need_total)  // (uncoalesced; optional output)
+              p.out_score[(size_t)(t0 + tt) * p.K + off + (slot - e_lo)] = key_score(key[4 * g + k]);
+            sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
+          }
         base += (int)((ttot >> (8 * g)) & 0xffu);
       }
       sel_run = base;
@@ -1087,7 +1092,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         report(p.status, kStatusDeviceCheck);
     }
     if (rank == 0) {
-      for (int r = need_total + tid; r < p.K; r += kThreads) out[r] = -1;
+      for (int r = need_total + tid; r < p.K; r += kThreads) {
+        out[r] = -1;
+        if (p.out_score) p.out_score[(size_t)(t0 + tt) * p.K + r] = -INFINITY;
+      }
       if (tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_total;
     }
   }
@@ -1220,6 +1228,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.k_pool = a.k_pool;
   p.q_sf = a.q_sf;
   p.k_sf = a.k_sf;
+  p.out_score = a.out_score;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(best_c * a.B * groups));

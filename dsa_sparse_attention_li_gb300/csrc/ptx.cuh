@@ -452,5 +452,9 @@ DSA_DEV uint32_t score_key(float s) {
   if ((b << 1) == 0) b = 0;  // fold -0.0 onto +0.0
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
+// Inverse of score_key (for keys of finite scores).
+DSA_DEV float key_score(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
 
 }  // namespace dsa

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 3
+#define DSA_ABI_VERSION 4
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -113,6 +113,8 @@ typedef struct {
   const uint8_t* q_sf;    /* [n_q][H_I][d_I/32] E8M0 group scales, MXFP8 only (else NULL) */
   const uint8_t* k_sf;    /* [num_pages][page_size][d_I/32] E8M0, MXFP8 only; the 4-byte
                              row of scales must be 4-byte aligned (d_I = 128)              */
+  float* out_score;       /* [n_q][K] fp32 score of each position in out_idx (-inf for the
+                             padding), or NULL: the candidates of a context-parallel shard  */
 } dsa_li_args;
 
 dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
@@ -190,6 +192,34 @@ dsa_status dsa_sfa_prefill(const dsa_sfa_args* args, dsa_stream_t stream);
  */
 #define DSA_SFA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
 dsa_status dsa_sfa_decode_static(const dsa_sfa_args* args, dsa_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------ */
+/* Context-parallel top-K merge                                                                */
+/* ------------------------------------------------------------------------------------------ */
+
+/*
+ * "Inference Optimization for Kimi K3.1 Pro", section 5 (local Top-K before communication): a
+ * long sequence's positions are split over S shards; each shard runs dsa_li_topk on its own
+ * range (with out_score) and the shards' (score, position) candidates are gathered -- the one
+ * exchange step -- and merged here.  For each query t the result is the first min(K, valid)
+ * candidates in the order (score descending, position ascending), emitted in ascending
+ * position order with -1 padding: the same set dsa_li_topk selects over the whole range, since
+ * every position's score does not depend on the split.
+ *   cand_idx   [S][n_q][K_in] shard-local positions (-1 = none); position + shard_offset[s] is
+ *              the sequence position (shards own disjoint ranges)
+ *   cand_score [S][n_q][K_in] their scores
+ * Supported: S * K_in <= 16384, K <= K_in * S.  Device pointers; asynchronous on stream.
+ */
+typedef struct {
+  int S, n_q, K_in, K;
+  const int32_t* cand_idx;
+  const float* cand_score;
+  const int32_t* shard_offset; /* [S] device array                                          */
+  int32_t* out_idx;            /* [n_q][K]                                                   */
+  int32_t* out_cnt;            /* [n_q] or NULL                                              */
+} dsa_topk_merge_args;
+
+dsa_status dsa_topk_merge(const dsa_topk_merge_args* args, dsa_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------ */
 /* Indexer Prolog                                                                              */

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     lib = dsa.load()
-    assert lib.dsa_abi_version() == 3
+    assert lib.dsa_abi_version() == 4
     assert dsa.status_string(0) == "DSA_OK"
     assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
     assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"
@@ -37,7 +37,8 @@ def test_abi_version_and_status_strings():
 
 def test_struct_layouts_match_header():
     """ctypes mirrors of the argument structs have the C sizes (x86_64 / aarch64 LP64)."""
-    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 13 * 8
+    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 14 * 8
+    assert ctypes.sizeof(dsa.MergeArgs) == 4 * 4 + 5 * 8
     assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8
     assert ctypes.sizeof(dsa.PrologArgs) == 10 * 4 + 2 * 4 + 16 * 8 + 8 + 8
 
@@ -165,3 +166,18 @@ def test_indexer_prolog_host_validation(over, code):
     if code == dsa.DSA_ERR_UNSUPPORTED or over.get("B") == 0 or "n_q" in over:
         assert lib.dsa_prolog_workspace_bytes(ctypes.byref(a)) == 0
     assert lib.dsa_indexer_prolog(None, None) == dsa.DSA_ERR_INVALID_ARG
+
+
+def test_topk_merge_host_validation():
+    lib = dsa.load()
+    a = dsa.MergeArgs()
+    a.S, a.n_q, a.K_in, a.K = 2, 3, 2048, 2048
+    for n in ("cand_idx", "cand_score", "shard_offset", "out_idx"):
+        setattr(a, n, 4096)
+    assert lib.dsa_topk_merge(None, None) == dsa.DSA_ERR_INVALID_ARG
+    a.S = 9
+    assert lib.dsa_topk_merge(ctypes.byref(a), None) == dsa.DSA_ERR_UNSUPPORTED  # 9 x 2048 > 16384
+    a.S, a.cand_idx = 2, None
+    assert lib.dsa_topk_merge(ctypes.byref(a), None) == dsa.DSA_ERR_INVALID_ARG
+    a.n_q = 0
+    assert lib.dsa_topk_merge(ctypes.byref(a), None) == dsa.DSA_OK  # nothing to merge

@@ -13,6 +13,7 @@ import torch
 
 import dsa_inputs as di
 import dsa_sparse_attention_li_gb300 as dsa
+import oracle
 from parity import (BF16_TOL, FP8_TOL, check_indices, check_sfa, integer_fp8, run_gpu,
                     sample_tokens, sfa_errors)
 
@@ -263,3 +264,40 @@ def test_full_size_workload_sampled(cuda_lib, name, exact, tol):
     check_sfa(inp_cpu, g, toks)            # attention alone, bf16 tolerance
     if not exact:
         print("%s: %d/%d index rows exact, near-ties %s" % (name, n_exact, len(toks), ties))
+
+
+# ------------------------------------------------------------------ context-parallel indexer
+
+@pytest.mark.parametrize("name,L,B,S", [("decode_int_4k", 4096, 2, 2), ("decode_32k", 9000, 2, 3),
+                                        ("decode_32k_mxfp8", 12800, 1, 4), ("decode_32k_fp8", 5000, 3, 2)])
+def test_context_parallel_shards_merge_to_the_full_selection(cuda_lib, name, L, B, S):
+    """Each shard (a page-aligned range of every sequence's positions, same for all sequences)
+    selects its own top-K with scores; merging the shards' candidates gives exactly the
+    unsharded selection (a position's score does not depend on the split).  Decode: the query
+    is the last position, so every shard's positions are visible to it."""
+    inp_cpu, inp = _small(name, seq_lens=[L] * B, n_new=[1] * B)
+    wl = inp_cpu["wl"]
+    full = run_gpu(inp)
+    pages = (L + 63) // 64
+    cuts = [round(pages * s / S) for s in range(S + 1)]
+    cand_idx = torch.empty((S, wl.n_q, wl.K), dtype=torch.int32, device="cuda")
+    cand_score = torch.empty((S, wl.n_q, wl.K), dtype=torch.float32, device="cuda")
+    offsets = []
+    for s in range(S):
+        lo, hi = cuts[s] * 64, min(L, cuts[s + 1] * 64)
+        offsets.append(lo)
+        pt = inp["pt_k"][:, cuts[s]:cuts[s + 1]].contiguous()
+        seq = torch.full((B,), hi - lo, dtype=torch.int32, device="cuda")
+        dsa.li_topk(inp["q_li"], inp["w"], inp["k_pool"], pt, seq, inp["q_start"], wl.K,
+                    q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"), q_sf=inp.get("q_sf"),
+                    k_sf=inp.get("k_sf"), out_idx=cand_idx[s], out_score=cand_score[s])
+    off = torch.tensor(offsets, dtype=torch.int32, device="cuda")
+    idx, cnt = dsa.topk_merge(cand_idx, cand_score, off, wl.K)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), full["idx"])
+    assert np.array_equal(cnt.cpu().numpy(), full["cnt"])
+    # the scores a shard reports are the oracle's (exact on the integer-valued config)
+    if name == "decode_int_4k":
+        s_or, _ = oracle.li_scores(inp_cpu, 0)
+        ci, cs = cand_idx[0, 0].cpu().numpy(), cand_score[0, 0].cpu().numpy()
+        assert np.array_equal(cs[ci >= 0], s_or[ci[ci >= 0]])
