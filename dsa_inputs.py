@@ -17,6 +17,9 @@ Layouts (all row-major, C order):
 * ``pt_k``     [B, max_pages]   int32 page table of the key cache
 * ``q_sfa``    [n_q, H, 576]    bf16 attention queries (512 latent + 64 rope)
 * ``kv_pool``  [pages_kv, 64, 576] bf16 paged MLA latent cache; the value is its first 512 columns
+* ``kv8_pool`` [pages_kv, 64, 608] uint8 FP8 latent cache (kv_dtype "fp8"): per row 576 e4m3
+               codes, then one fp32 scale per 128-column tile (5; the last tile is the 64 rope
+               columns), then 12 zero bytes
 * ``pt_kv``    [B, max_pages]   int32 page table of the latent cache
 * ``seq_lens`` [B] int32 positions per sequence, new tokens included
 * ``q_start``  [B+1] int32 prefix offsets of each sequence's query tokens
@@ -59,6 +62,7 @@ class Workload:
     softmax_scale: float = field(default=1.0 / math.sqrt(D_QK))
     d_q: int = 1536                 # Indexer Prolog: input width of the Q projection
     d_model: int = 7168             # Indexer Prolog: input width of the K / head-weight projections
+    kv_dtype: str = "bf16"          # latent cache: "bf16" | "fp8" (per-token, 128-column tiles)
 
     @property
     def B(self) -> int:
@@ -186,6 +190,26 @@ def _int_mx(x: torch.Tensor, g: torch.Generator):
     return x.to(torch.float8_e4m3fn), sf
 
 
+KV8_ROW = 608
+KV8_TILE = 128
+
+
+def _quant_kv8(rows: torch.Tensor) -> torch.Tensor:
+    """FP8 latent-cache rows from fp32 rows [N, 576]: per row and 128-column tile, scale =
+    amax/448 (1 when amax == 0), codes = e4m3(x / scale) (nearest even, clamped); packed as 576
+    code bytes, 5 fp32 scales, 12 zero bytes."""
+    n, d = rows.shape
+    out = torch.zeros((n, KV8_ROW), dtype=torch.uint8, device=rows.device)
+    for i, c0 in enumerate(range(0, d, KV8_TILE)):
+        tile = rows[:, c0:c0 + KV8_TILE]
+        amax = tile.abs().amax(1, keepdim=True)
+        scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+        codes = (tile / scale).clamp(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+        out[:, c0:c0 + tile.shape[1]] = codes.view(torch.uint8)
+        out[:, d + 4 * i:d + 4 * i + 4] = scale.to(torch.float32).view(torch.uint8).view(n, 4)
+    return out
+
+
 def _page_table(pages: List[int], max_pages: int, g: torch.Generator) -> torch.Tensor:
     total = sum(pages)
     perm = torch.randperm(total, generator=g).to(torch.int32)
@@ -268,7 +292,11 @@ def generate(wl: Workload, device="cpu") -> dict:
 
     # attention queries and the latent cache
     out["q_sfa"] = _draw((n_q, wl.H, wl.d_qk), wl.values, gv, device).to(torch.bfloat16)
-    out["kv_pool"] = _paged_fill(wl, pt_kv, wl.d_qk, wl.values, gv, device).to(torch.bfloat16)
+    kv = _paged_fill(wl, pt_kv, wl.d_qk, wl.values, gv, device)
+    out["kv_pool"] = kv.to(torch.bfloat16)
+    if wl.kv_dtype == "fp8":
+        out["kv8_pool"] = _quant_kv8(kv.view(-1, wl.d_qk)).view(wl.num_pages, wl.page_size, KV8_ROW)
+    del kv
 
     out["pt_k"] = pt_k.to(device)
     out["pt_kv"] = pt_kv.to(device)
@@ -352,7 +380,8 @@ def repage(inp: dict, seed: int) -> dict:
     wl = inp["wl"]
     g = torch.Generator().manual_seed(seed)
     out = dict(inp)
-    for pool_key, pt_key, sc_keys in (("k_pool", "pt_k", ("k_scale", "k_sf")), ("kv_pool", "pt_kv", ())):
+    for pool_key, pt_key, sc_keys in (("k_pool", "pt_k", ("k_scale", "k_sf")),
+                                      ("kv_pool", "pt_kv", ("kv8_pool",))):
         old_pt = inp[pt_key].cpu()
         new_pt = _page_table(wl.pages(), wl.max_pages, g)
         pool = inp[pool_key]

@@ -38,7 +38,7 @@ class _Sfa(ctypes.Structure):
                 ("B", "n_q", "H", "d_qk", "d_v", "K", "page_size", "max_pages", "num_pages")] + [
         ("scale", ctypes.c_double), ("q", ctypes.c_void_p), ("kv_pool", ctypes.c_void_p),
         ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
-        ("q_start", ctypes.c_void_p)]
+        ("q_start", ctypes.c_void_p), ("kv_fp8", ctypes.c_int), ("kv8_pool", ctypes.c_void_p)]
 
 
 def lib():
@@ -105,6 +105,8 @@ def _sfa_struct(inp, K, keep):
     s.page_table = keep.ptr(inp["pt_kv"])
     s.seq_lens = keep.ptr(inp["seq_lens"])
     s.q_start = keep.ptr(inp["q_start"])
+    s.kv_fp8 = 1 if getattr(wl, "kv_dtype", "bf16") == "fp8" else 0
+    s.kv8_pool = keep.ptr(inp.get("kv8_pool"))
     return s
 
 
@@ -215,6 +217,16 @@ def decode_bf16(bits: int) -> float:
     f.argtypes = [ctypes.c_uint16]
     f.restype = ctypes.c_double
     return f(bits)
+
+
+def decode_kv8(row, d: int) -> float:
+    """Element d of one FP8 latent-cache row (608 bytes: 576 e4m3 codes, 5 fp32 tile scales)."""
+    row = np.ascontiguousarray(np.asarray(row, dtype=np.uint8))
+    assert row.shape == (608,)
+    f = lib().orc_kv8_element
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    f.restype = ctypes.c_double
+    return f(row.ctypes.data, d)
 
 
 def decode_e8m0(bits: int) -> float:

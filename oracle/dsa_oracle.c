@@ -79,6 +79,10 @@ typedef struct {
   const int* page_table;      /* [B][max_pages]                                         */
   const int* seq_lens;        /* [B]                                                    */
   const int* q_start;         /* [B+1]                                                  */
+  int kv_fp8;                 /* 1: the latent cache is FP8 rows (kv8_pool), else bf16    */
+  const uint8_t* kv8_pool;    /* [num_pages][page_size][608]: 576 e4m3 codes, then one
+                                 fp32 scale per 128-column tile (5; the last tile is the 64
+                                 rope columns), then 12 bytes of padding                   */
 } orc_sfa;
 
 /* ---- number formats, from their definitions ------------------------------------------ */
@@ -107,6 +111,21 @@ double orc_e4m3(uint8_t bits) {
 double orc_e8m0(uint8_t bits) {
   if (bits == 0xFF) return NAN;
   return ldexp(1.0, (int)bits - 127);
+}
+
+static uint16_t orc_bf16_encode(double v);
+
+/* FP8 latent cache ("Inference Optimization for Kimi K3.1 Pro", section 4, SFA KV cache
+ * quantisation: the cache is stored in FP8 with one scale per token and 128-column tile, and
+ * the attention arithmetic runs on the de-quantised BF16 values).  Element d of a row is the
+ * e4m3 code times its tile's fp32 scale, the product rounded to fp32 and then to bf16 (the
+ * precision in which a BF16 tensor-core operand is formed from the stored pair). */
+#define ORC_KV8_ROW 608
+double orc_kv8_element(const uint8_t* row, int d) {
+  float sc;
+  memcpy(&sc, row + 576 + 4 * (d / 128), sizeof sc);
+  const float prod = (float)orc_e4m3(row[d]) * sc;
+  return orc_bf16(orc_bf16_encode((double)prod));
 }
 
 /* ---- token -> (sequence, position) and position -> physical row ---------------------- */
@@ -263,9 +282,17 @@ int oracle_li_topk(const orc_li* P, int n_tok, const int* toks, int* out_idx, in
 static int sfa_check(const orc_sfa* S) {
   if (!S || S->B <= 0 || S->n_q < 0 || S->H <= 0 || S->d_qk <= 0 || S->d_v <= 0 ||
       S->d_v > S->d_qk || S->K <= 0 || S->page_size <= 0 || S->max_pages <= 0 || !S->q ||
-      !S->kv_pool || !S->page_table || !S->seq_lens || !S->q_start)
+      !(S->kv_fp8 ? (const void*)S->kv8_pool : (const void*)S->kv_pool) || !S->page_table ||
+      !S->seq_lens || !S->q_start)
     return ORC_EARG;
+  if (S->kv_fp8 && S->d_qk != 576) return ORC_EARG;
   return ORC_OK;
+}
+
+/* Element d of the latent row at physical row `row` (bf16 cache, or de-quantised FP8 row). */
+static double sfa_kv(const orc_sfa* S, long long row, int d) {
+  if (S->kv_fp8) return orc_kv8_element(S->kv8_pool + row * ORC_KV8_ROW, d);
+  return orc_bf16(S->kv_pool[row * S->d_qk + d]);
 }
 
 /* out[i][h][0..d_v) and lse[i][h] for each listed token over its K indices (entries -1 are
@@ -307,9 +334,9 @@ int oracle_sfa(const orc_sfa* S, int n_tok, const int* toks, const int* idx, dou
       for (int r = 0; r < S->K; ++r) {
         int j = set[r];
         if (j < 0) continue;
-        const uint16_t* kv = S->kv_pool + phys_row(S->page_table, S->max_pages, S->page_size, b, j) * S->d_qk;
+        const long long row = phys_row(S->page_table, S->max_pages, S->page_size, b, j);
         double dot = 0.0;
-        for (int d = 0; d < S->d_qk; ++d) dot += orc_bf16(qh[d]) * orc_bf16(kv[d]);
+        for (int d = 0; d < S->d_qk; ++d) dot += orc_bf16(qh[d]) * sfa_kv(S, row, d);
         z[r] = S->scale * dot;
         if (z[r] > zmax) zmax = z[r];
       }
@@ -318,10 +345,10 @@ int oracle_sfa(const orc_sfa* S, int n_tok, const int* toks, const int* idx, dou
       for (int r = 0; r < S->K; ++r) {
         int j = set[r];
         if (j < 0) continue;
-        const uint16_t* kv = S->kv_pool + phys_row(S->page_table, S->max_pages, S->page_size, b, j) * S->d_qk;
+        const long long row = phys_row(S->page_table, S->max_pages, S->page_size, b, j);
         double a = exp(z[r] - zmax);
         denom += a;
-        for (int d = 0; d < S->d_v; ++d) o[d] += a * orc_bf16(kv[d]);
+        for (int d = 0; d < S->d_v; ++d) o[d] += a * sfa_kv(S, row, d);
       }
       if (denom > 0.0)
         for (int d = 0; d < S->d_v; ++d) o[d] /= denom;

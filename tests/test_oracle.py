@@ -392,6 +392,57 @@ def test_prolog_encodings_and_cache_rows():
     assert np.array_equal(rb["q_enc"], qb)  # integers below 2^8 are exact in bf16
 
 
+# ---------------------------------------------------------------- FP8 latent cache
+
+def test_kv8_row_hand_decoding():
+    g = _gold("kv8_hand_row.json")
+    row = np.zeros(608, dtype=np.uint8)
+    row[576:596] = np.array(g["scales"], dtype=np.float32).view(np.uint8)
+    for e in g["elements"]:
+        row[e["d"]] = e["code"]
+    for e in g["elements"]:
+        assert oracle.decode_kv8(row, e["d"]) == e["value"], e
+    assert oracle.decode_kv8(row, 2) == 0.0  # code 0
+
+
+def test_sfa_on_fp8_cache_equals_bf16_cache_of_the_dequantised_values():
+    """Power-of-two tile scales and small integer codes de-quantise exactly, so attention over
+    the FP8 rows must equal the pinned bf16 attention over a cache holding those values."""
+    wl = di.Workload("kv8", [70, 130], [1, 2], H_I=2, d_I=8, K=16, H=3, values="int4", seed=51,
+                     kv_dtype="fp8")
+    inp = di.generate(wl)
+    g = torch.Generator().manual_seed(9)
+    n = wl.num_pages * wl.page_size
+    codes = torch.randint(-6, 7, (n, 576), generator=g).float()
+    scales = 2.0 ** torch.randint(-3, 3, (n, 5), generator=g).float()
+    rows = torch.zeros((n, 608), dtype=torch.uint8)
+    rows[:, :576] = codes.to(torch.float8_e4m3fn).view(torch.uint8)
+    rows[:, 576:596] = scales.contiguous().view(torch.uint8).view(n, 20)
+    vals = codes * scales.repeat_interleave(128, 1)[:, :576]
+    kv8 = dict(inp, kv8_pool=rows.view(wl.num_pages, wl.page_size, 608))
+    bf = dict(inp, wl=di.Workload(**{**wl.__dict__, "kv_dtype": "bf16"}),
+              kv_pool=vals.to(torch.bfloat16).view(wl.num_pages, wl.page_size, 576))
+    assert torch.equal(vals.to(torch.bfloat16).float(), vals)  # exactly representable
+    sets = [[0, 5, 33, 69, -1, 12], [129, 64, 1, -1, -1, 100], [7, 8, 9, 10, 128, 127]]
+    a, b = oracle.sfa(kv8, sets), oracle.sfa(bf, sets)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_kv8_generator_tiles():
+    """Each tile's largest code is +-448 (scale = amax / 448), and de-quantised rows stay within
+    e4m3's half step (2^-4 relative) of the bf16 cache they were made from."""
+    wl = di.small("decode_32k", seq_lens=[200], n_new=[1], kv_dtype="fp8")
+    inp = di.generate(wl)
+    rows = inp["kv8_pool"].view(-1, 608)
+    codes = rows[:, :576].view(torch.float8_e4m3fn).float()
+    for i in range(5):
+        assert torch.all(codes[:, 128 * i:128 * (i + 1)].abs().amax(1) == 448)
+    ref = inp["kv_pool"].view(-1, 576).float()
+    r = rows[:4].numpy()
+    got = torch.tensor([[oracle.decode_kv8(r[k], d) for d in range(576)] for k in range(4)])
+    assert torch.all((got - ref[:4]).abs() <= ref[:4].abs() * 2.0 ** -4 * 1.01 + 2.0 ** -12)
+
+
 # ---------------------------------------------------------------- top-K: definition by brute force
 
 def _check_selection(s, idx_row, cnt, K):
