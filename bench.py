@@ -523,7 +523,7 @@ def run_prolog(args):
                    "l2": "L2 flushed (256 MB write) before every timed launch; per-launch CUDA events",
                    "launch": "one C-ABI launch per step (three CTA roles)"},
         "roofline": {"kernel": "prolog", "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": gbs / hbm, "peak_kind": peak_kind, "traffic": None,
+                     "frac": gbs / hbm, "peak_kind": peak_kind, "traffic": committed_traffic(wl.name),
                      "algorithmic_bytes": bytes_},
         "kernels": {"prolog_us": us, "prolog_tflops": flop / (us * 1e-6) / 1e12},
         "gpu_launches": K, "clocks": clk.summary(),
