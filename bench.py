@@ -60,7 +60,7 @@ def algorithmic(wl, cnt_total):
     # key scales: one fp32 per row (fp8), one E8M0 byte per 32 elements (mxfp8)
     sc = {"bf16": 0, "fp8": 4, "mxfp8": wl.d_I // 32}[wl.li_dtype]
     k_bytes = pages * P * (wl.d_I * elt + sc)
-    gather_bytes = cnt_total * wl.d_qk * 2
+    gather_bytes = cnt_total * (608 if wl.kv_dtype == "fp8" else wl.d_qk * 2)  # bytes per row
     li_flop = 0
     for L, n in zip(wl.seq_lens, wl.n_new):
         li_flop += sum(2 * (L - n + i + 1) * wl.H_I * wl.d_I for i in range(n))
@@ -257,7 +257,8 @@ def run_ours(args):
                                k_scale=inp.get("k_scale"), max_seq_len=ms, max_q_per_seq=mq,
                                out_idx=idx, out_cnt=cnt, status=status, q_sf=inp.get("q_sf"),
                                k_sf=inp.get("k_sf"))
-    sfa_args = dsa.sfa_args(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"],
+    kv = inp["kv8_pool"] if wl.kv_dtype == "fp8" else inp["kv_pool"]
+    sfa_args = dsa.sfa_args(inp["q_sfa"], kv, inp["pt_kv"], inp["seq_lens"],
                             inp["q_start"], idx, softmax_scale=wl.softmax_scale, max_seq_len=ms,
                             max_q_per_seq=mq, out=out, lse=lse, status=status, workspace=ws)
     stream = torch.cuda.Stream(device=dev)
@@ -360,7 +361,7 @@ def run_ours(args):
                                 max_seq_len=ms, max_q_per_seq=mq, out_idx=o["idx"], out_cnt=o["cnt"],
                                 status=status, q_sf=d.get("q_sf"), k_sf=inp.get("k_sf"))
                for d, o in zip(din, dout)]
-        sfa2 = [dsa.sfa_args(d["q_sfa"], inp["kv_pool"], d["pt_kv"], d["seq_lens"], d["q_start"], o["idx"],
+        sfa2 = [dsa.sfa_args(d["q_sfa"], kv, d["pt_kv"], d["seq_lens"], d["q_start"], o["idx"],
                              softmax_scale=wl.softmax_scale, max_seq_len=ms, max_q_per_seq=mq,
                              out=o["out"], lse=o["lse"], status=status, workspace=ws)
                 for d, o in zip(din, dout)]
@@ -423,7 +424,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {**wl.describe(), "l2": "inputs larger than L2: every step streams %.0f MB of key pages "
                    "and gathers from a %.0f MB latent pool" % (work["k_bytes"] / 1e6,
-                                                               inp["kv_pool"].numel() * 2 / 1e6),
+                                                               kv.numel() * kv.element_size() / 1e6),
                    "launch": "eager C-ABI calls on one stream; the attention kernel is a programmatic dependent launch; per-kernel CUDA events on every 8th step"},
         "roofline": {"kernel": "li_topk", "bound": "hbm", "achieved": li_achieved, "peak": hbm,
                      "unit": "GB/s", "frac": li_achieved / hbm, "peak_kind": peak_kind,

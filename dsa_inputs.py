@@ -87,7 +87,7 @@ class Workload:
         return {
             "workload": self.name, "B": self.B, "n_q": self.n_q, "H_I": self.H_I, "d_I": self.d_I,
             "K": self.K, "H": self.H, "d_qk": self.d_qk, "d_v": self.d_v, "page": self.page_size,
-            "li_dtype": self.li_dtype, "values": self.values,
+            "li_dtype": self.li_dtype, "kv_dtype": self.kv_dtype, "values": self.values,
             "seq_len_min": min(self.seq_lens), "seq_len_max": max(self.seq_lens),
             "positions": sum(self.seq_lens), "seed": self.seed,
         }
@@ -108,6 +108,7 @@ def preset(name: str) -> Workload:
     decode_32k      : 32 sequences x 1 token, L=32768, 64x128 index heads, K=2048, 128 heads
     decode_32k_fp8  : decode_32k with e4m3 index q/k and per-token fp32 scales
     decode_32k_mxfp8: decode_32k with MXFP8 index q/k (e4m3 elements, one E8M0 scale per 32)
+    decode_32k_kv8  : decode_32k with the FP8 latent cache (per-token 128-column tile scales)
     prolog_decode_32k: the Indexer Prolog of decode_32k_mxfp8's 32 new tokens (Q projection from
                       a 1536-wide query input, K and head weights from a 7168-wide hidden state)
     specdec_ragged  : 64 sequences x 2 tokens (verified + draft), L log-uniform in [1024, 131072]
@@ -127,6 +128,9 @@ def preset(name: str) -> Workload:
     if name == "prolog_decode_32k":
         return Workload(name, [32768] * 32, [1] * 32, H_I=64, d_I=128, K=2048, H=128,
                         li_dtype="mxfp8", seed=1007)
+    if name == "decode_32k_kv8":
+        return Workload(name, [32768] * 32, [1] * 32, H_I=64, d_I=128, K=2048, H=128,
+                        kv_dtype="fp8", seed=1008)
     if name == "specdec_ragged":
         lens = _log_uniform_lengths(64, 1024, 131072, seed=1004)
         return Workload(name, lens, [2] * 64, H_I=64, d_I=128, K=2048, H=128, seed=1004)
@@ -135,8 +139,8 @@ def preset(name: str) -> Workload:
     raise KeyError(name)
 
 
-PRESETS = ["decode_int_4k", "decode_32k", "decode_32k_fp8", "decode_32k_mxfp8", "specdec_ragged",
-           "prefill_64k"]
+PRESETS = ["decode_int_4k", "decode_32k", "decode_32k_fp8", "decode_32k_mxfp8", "decode_32k_kv8",
+           "specdec_ragged", "prefill_64k"]
 
 
 def small(name: str, **over) -> Workload:

@@ -73,7 +73,7 @@ class SfaArgs(ctypes.Structure):
         "B", "n_q", "H", "d_qk", "d_v", "K", "page_size", "max_pages", "num_pages", "max_seq_len",
         "max_q_per_seq")] + [("softmax_scale", ctypes.c_float)] + [(n, ctypes.c_void_p) for n in (
             "q", "kv_pool", "page_table", "seq_lens", "q_start", "idx", "out", "lse", "status",
-            "workspace")] + [("workspace_bytes", ctypes.c_size_t)]
+            "workspace")] + [("workspace_bytes", ctypes.c_size_t), ("kv_dtype", ctypes.c_int)]
 
 
 _lib = None
@@ -212,6 +212,8 @@ def sfa_args(q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax_scale, m
     a.idx, a.out, a.lse, a.status = _ptr(idx), _ptr(out), _ptr(lse), _ptr(status)
     a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    # a uint8 pool holds FP8 rows (576 e4m3 codes + 5 fp32 tile scales + padding = 608 bytes)
+    a.kv_dtype = DSA_FP8_E4M3 if kv_pool.dtype == torch.uint8 else DSA_BF16
     return a
 
 
@@ -385,7 +387,8 @@ def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=
                        max_seq_len=ms, max_q_per_seq=mq, out_idx=idx, out_cnt=cnt, status=status,
                        stream=stream, q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf"))
     f = sfa_prefill if prefill else sfa_decode
-    out, lse = f(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"], inp["q_start"], idx,
+    kv = inp["kv8_pool"] if getattr(wl, "kv_dtype", "bf16") == "fp8" else inp["kv_pool"]
+    out, lse = f(inp["q_sfa"], kv, inp["pt_kv"], inp["seq_lens"], inp["q_start"], idx,
                  softmax_scale=inp["softmax_scale"], max_seq_len=ms, max_q_per_seq=mq, out=out,
                  lse=lse, status=status, workspace=workspace, stream=stream)
     return idx, cnt, out, lse

@@ -192,6 +192,8 @@ static dsa_status sfa_common(const dsa_sfa_args* a, bool prefill, dsa_stream_t s
   if (a->d_qk != 576 || a->d_v != 512)
     return fail(DSA_ERR_UNSUPPORTED, std::string(name) + ": d_qk must be 576 and d_v 512");
   if (a->page_size != 64) return fail(DSA_ERR_UNSUPPORTED, std::string(name) + ": page_size must be 64");
+  if (a->kv_dtype != DSA_BF16 && a->kv_dtype != DSA_FP8_E4M3)
+    return fail(DSA_ERR_UNSUPPORTED, std::string(name) + ": kv_dtype must be BF16 or FP8_E4M3");
   if (a->H > 128) return fail(DSA_ERR_UNSUPPORTED, std::string(name) + ": H > 128");
   if (a->K > 2048) return fail(DSA_ERR_UNSUPPORTED, std::string(name) + ": K > 2048");
   std::string err;

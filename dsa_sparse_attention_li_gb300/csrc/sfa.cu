@@ -175,6 +175,18 @@ DSA_DEV uint32_t stage_chunk_offset(int ch, int rr) {
                  : (uint32_t)(4 * kBoxBytes + rr * 64 + ((((ch - 32) ^ (rr >> 1)) & 3) << 4));
 }
 
+// FP8 latent rows: 576 e4m3 codes, one fp32 scale per 128-column tile (5), padding to 608 B.
+constexpr int kKv8Row = 608;
+
+// Two e4m3 codes (low byte first) times their tile scale: fp32 products rounded to nearest, then
+// packed as two bf16 rounded to nearest even.
+DSA_DEV uint32_t dequant2(uint32_t codes2, float scale) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)codes2, __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16(f.x * scale, f.y * scale);
+}
+
+template <bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
                const Params p) {
@@ -318,19 +330,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*reinterpret_cast<volatile int*>(&ctl->gather_go[i & 1]) == 0) break;
       }
       const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
+      if constexpr (KV8) {
+        // FP8 rows ("Inference Optimization for Kimi K3.1 Pro", section 4: the cache is FP8
+        // with a scale per token and 128-column tile, the attention arithmetic BF16): each
+        // 16-byte operand chunk is 8 codes of the row times their tile scale, converted in
+        // registers and stored swizzled; empty slots store zeros.  Six chunks' loads in flight.
+        uint8_t* stage = st_s + (size_t)s * kTileBytes;
 #pragma unroll
-      for (int k = 0; k < kGatherPer; ++k) {
-        const int c = g + k * kGatherThreads;
-        if (c < kChunks) {
-          const int r = c / kRowChunks, ch = c % kRowChunks;
-          const int slot = i * kNT + r;
-          const int row = slot < nslot ? rows_s[slot] : -1;
-          const uint32_t dst = base + stage_chunk_offset(ch, r);
-          const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + row_chunk_offset(ch, half) : kv;
-          cp_async16(dst, src, row >= 0 ? 16u : 0u);
+        for (int k0 = 0; k0 < kGatherPer; k0 += 6) {
+          uint2 code[6];
+          float sc[6];
+          uint32_t off[6];
+#pragma unroll
+          for (int u = 0; u < 6; ++u) {
+            const int c = g + (k0 + u) * kGatherThreads;
+            code[u] = make_uint2(0u, 0u);
+            sc[u] = 0.f;
+            off[u] = 0xffffffffu;
+            if (k0 + u < kGatherPer && c < kChunks) {
+              const int r = c / kRowChunks, ch = c % kRowChunks;
+              const int slot = i * kNT + r;
+              const int row = slot < nslot ? rows_s[slot] : -1;
+              off[u] = stage_chunk_offset(ch, r);
+              if (row >= 0) {
+                const int e = row_chunk_offset(ch, half) >> 1;  // first of the chunk's 8 columns
+                const uint8_t* rp = kv + (size_t)row * kKv8Row;
+                code[u] = __ldg(reinterpret_cast<const uint2*>(rp + e));
+                sc[u] = __ldg(reinterpret_cast<const float*>(rp + kDqk + 4 * (e >> 7)));
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 6; ++u)
+            if (off[u] != 0xffffffffu)
+              *reinterpret_cast<uint4*>(stage + off[u]) =
+                  make_uint4(dequant2(code[u].x & 0xffffu, sc[u]), dequant2(code[u].x >> 16, sc[u]),
+                             dequant2(code[u].y & 0xffffu, sc[u]), dequant2(code[u].y >> 16, sc[u]));
         }
+        fence_proxy_async_smem();  // generic-proxy stores -> the tensor core's reads
+        mbar_arrive(&ctl->full[s]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kGatherPer; ++k) {
+          const int c = g + k * kGatherThreads;
+          if (c < kChunks) {
+            const int r = c / kRowChunks, ch = c % kRowChunks;
+            const int slot = i * kNT + r;
+            const int row = slot < nslot ? rows_s[slot] : -1;
+            const uint32_t dst = base + stage_chunk_offset(ch, r);
+            const uint8_t* src = row >= 0 ? kv + (size_t)row * (kDqk * 2) + row_chunk_offset(ch, half) : kv;
+            cp_async16(dst, src, row >= 0 ? 16u : 0u);
+          }
+        }
+        cp_async_arrive_noinc(&ctl->full[s]);
       }
-      cp_async_arrive_noinc(&ctl->full[s]);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kMmaWarp && lane == 0) {
@@ -916,8 +969,13 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   }
   if (a.n_q == 0) return DSA_OK;
 
+  const bool kv8 = a.kv_dtype == DSA_FP8_E4M3;
   const char* simple = std::getenv("DSA_SFA_CUDA_CORE");
   if (simple && simple[0] == '1') {
+    if (kv8) {
+      err = "sfa (cuda-core): bf16 latent cache only";
+      return DSA_ERR_UNSUPPORTED;
+    }
     sfa_cuda_core_kernel<<<a.n_q * a.H, 128, 0, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "sfa (cuda-core): launch", err);
@@ -931,7 +989,8 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
                       kDqk * 2, kRopeHalf, kHeads, CU_TENSOR_MAP_SWIZZLE_64B, err))
     return DSA_ERR_CUDA;
   const int smem = Layout::total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(sfa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = kv8 ? sfa_kernel<true> : sfa_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "sfa: set shared memory size", err);
   const unsigned grid = (unsigned)(a.n_q * 2 * pl.splits);
   if (std::getenv("DSA_VERBOSE"))
@@ -954,7 +1013,7 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, sfa_kernel, tm_q, tm_qr, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_q, tm_qr, p);
   if (e != cudaSuccess) return cuda_fail(e, "sfa: launch", err);
   return DSA_OK;
 }

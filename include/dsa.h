@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 4
+#define DSA_ABI_VERSION 5
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -144,7 +144,13 @@ dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
  * is therefore kept for every input, whichever kernel wrote it.
  *
  * Supported: page_size 64; d_qk 576; d_v 512; H in {16, 128} (decode) and 128 (prefill);
- * 1 <= K <= 2048; bf16 q/kv/out.
+ * 1 <= K <= 2048; bf16 q/out; latent cache bf16 or FP8 (kv_dtype).
+ *
+ * FP8 latent cache (kv_dtype DSA_FP8_E4M3; "Inference Optimization for Kimi K3.1 Pro",
+ * section 4, SFA KV cache quantisation per token and 128-column tile): each row of kv_pool is
+ * 608 bytes: the 576 columns as e4m3 codes, then one fp32 scale per 128-column tile (5; the
+ * last covers the 64 rope columns), then 12 unused bytes.  The attention runs on the BF16
+ * values bf16(fp32(code * scale)) (both roundings to nearest even).
  */
 typedef struct {
   int B, n_q;
@@ -165,6 +171,7 @@ typedef struct {
   int32_t* status;           /* device int32 error word, or NULL                         */
   void* workspace;           /* device scratch of dsa_sfa_workspace_bytes(), 256-B aligned */
   size_t workspace_bytes;
+  dsa_dtype kv_dtype;        /* DSA_BF16 (rows of 576 bf16) or DSA_FP8_E4M3 (608-byte rows) */
 } dsa_sfa_args;
 
 /* Scratch that dsa_sfa_decode needs for these arguments (0 if none).  Host only, no CUDA. */

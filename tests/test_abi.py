@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     lib = dsa.load()
-    assert lib.dsa_abi_version() == 4
+    assert lib.dsa_abi_version() == 5
     assert dsa.status_string(0) == "DSA_OK"
     assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
     assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"
@@ -39,7 +39,7 @@ def test_struct_layouts_match_header():
     """ctypes mirrors of the argument structs have the C sizes (x86_64 / aarch64 LP64)."""
     assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 14 * 8
     assert ctypes.sizeof(dsa.MergeArgs) == 4 * 4 + 5 * 8
-    assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8
+    assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8 + 8
     assert ctypes.sizeof(dsa.PrologArgs) == 10 * 4 + 2 * 4 + 16 * 8 + 8 + 8
 
 

@@ -301,3 +301,23 @@ def test_context_parallel_shards_merge_to_the_full_selection(cuda_lib, name, L, 
         s_or, _ = oracle.li_scores(inp_cpu, 0)
         ci, cs = cand_idx[0, 0].cpu().numpy(), cand_score[0, 0].cpu().numpy()
         assert np.array_equal(cs[ci >= 0], s_or[ci[ci >= 0]])
+
+
+# ------------------------------------------------------------------ FP8 latent cache
+
+@pytest.mark.parametrize("name,lens,new,prefill,K", [
+    ("decode_32k", [5000, 2100, 777], [1, 2, 1], False, None),
+    ("decode_int_4k", [4096, 700], [1, 2], False, None),
+    ("prefill_64k", [3000], [300], True, 256)])
+def test_fp8_latent_cache_attention(cuda_lib, name, lens, new, prefill, K):
+    """Attention over FP8 latent rows (e4m3 codes, fp32 scale per 128-column tile) against the
+    oracle on the same rows, de-quantised as bf16(fp32(code * scale))."""
+    over = dict(seq_lens=lens, n_new=new, kv_dtype="fp8")
+    if K:
+        over["K"] = K
+    inp_cpu, inp = _small(name, **over)
+    g = run_gpu(inp, prefill=prefill)
+    assert g["status"] == 0
+    toks = sample_tokens(inp_cpu["wl"], 12, seed=4)
+    check_indices(inp_cpu, g, toks, exact=name == "decode_int_4k")
+    check_sfa(inp_cpu, g, toks)
