@@ -1070,17 +1070,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every lane's keys of the batch are in registers (the scan above), and the staged count
       // never exceeds the keys read so far: the writes land on keys already consumed
       int base = sel_run;
+      if (p.out_score == nullptr) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
+        for (int g = 0; g < 4; ++g) {
+          int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if ((take >> (4 * g + k)) & 1u) {
-            if (p.out_score && off + (slot - e_lo) < need_total)  // (uncoalesced; optional output)
-              p.out_score[(size_t)(t0 + tt) * p.K + off + (slot - e_lo)] = key_score(key[4 * g + k]);
-            sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
-          }
-        base += (int)((ttot >> (8 * g)) & 0xffu);
+          for (int k = 0; k < 4; ++k)
+            if ((take >> (4 * g + k)) & 1u) sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
+          base += (int)((ttot >> (8 * g)) & 0xffu);
+        }
+      } else {  // also the score of each selected position (uncoalesced; optional output)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if ((take >> (4 * g + k)) & 1u) {
+              if (off + (slot - e_lo) < need_total)
+                p.out_score[(size_t)(t0 + tt) * p.K + off + (slot - e_lo)] = key_score(key[4 * g + k]);
+              sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
+            }
+          base += (int)((ttot >> (8 * g)) & 0xffu);
+        }
       }
       sel_run = base;
     }
