@@ -639,3 +639,14 @@ def test_sfa_rejects_out_of_range_index():
     inp = _random_sfa(35)
     with pytest.raises(ValueError):
         oracle.sfa(inp, [[50, -1], [0, 1], [0, 1]])
+
+
+def test_fp8_latent_cache_page_permutation_invariance():
+    wl = di.Workload("kv8p", [90, 150], [1, 2], H_I=2, d_I=8, K=16, H=2, seed=61, d_qk=576,
+                     d_v=512, page_size=16, kv_dtype="fp8")
+    inp = di.generate(wl)
+    inp2 = di.repage(inp, seed=5)
+    assert not torch.equal(inp["pt_kv"], inp2["pt_kv"])
+    sets = [[0, 3, 89, -1], [5, 149, 77, 100], [1, 2, 148, 149]]
+    a, b = oracle.sfa(inp, sets), oracle.sfa(inp2, sets)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
