@@ -11,6 +11,7 @@ Functions:
   sfa(inp, idx, tokens)      -> (out [n, H, d_v] float64, lse [n, H] float64)
   prolog(inp)                -> Indexer Prolog outputs (projections, LayerNorm, quantisation)
   mx_quantize(v)             -> OCP MX e4m3 codes and E8M0 scale bytes of a vector
+  decode_kv8(row, d)         -> element d of one FP8 latent-cache row (608 bytes)
 ``inp`` is the dict produced by ``dsa_inputs.generate`` (tensors moved to the CPU on demand).
 """
 import ctypes

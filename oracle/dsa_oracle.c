@@ -37,7 +37,10 @@
  *              ascending); emitted in ascending position order, then -1 padding.
  *   attention  z_j = scale * q[t,h,0:576] . kv[j,0:576];  o = sum_j softmax(z)_j kv[j,0:512];
  *              lse = max z + log(sum exp(z - max z)) (natural log).  An empty index set gives
- *              o = 0 and lse = -inf.
+ *              o = 0 and lse = -inf.  With an FP8 latent cache kv[j,d] is the de-quantised
+ *              bf16(fp32(e4m3 code * tile scale)), one fp32 scale per row and 128 columns.
+ *   prolog     projections, LayerNorm and OCP MX quantisation of the indexer's inputs (see
+ *              the Indexer Prolog section below).
  *
  * Parity pins (tests/test_oracle.py) tie each function to something other than itself: a
  * hand-worked example, closed forms, library routines (torch's fp8/bf16 decoders and dense

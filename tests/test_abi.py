@@ -118,6 +118,7 @@ def _sfa(**over):
     ({"d_qk": 512}, dsa.DSA_ERR_UNSUPPORTED),
     ({"H": 256}, dsa.DSA_ERR_UNSUPPORTED),
     ({"K": 4096}, dsa.DSA_ERR_UNSUPPORTED),
+    ({"kv_dtype": dsa.DSA_MXFP8_E4M3}, dsa.DSA_ERR_UNSUPPORTED),  # latent cache: bf16 or FP8 rows
 ])
 @pytest.mark.parametrize("entry", ["dsa_sfa_decode", "dsa_sfa_prefill"])
 def test_sfa_host_validation(over, code, entry):
