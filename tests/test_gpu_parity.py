@@ -1,6 +1,6 @@
 """Parity of the CUDA path (called through the C ABI) with the CPU oracle on seeded inputs.
 
-Small cases span several 128-key tiles, several CTAs of a cluster and ragged tails; the five
+Small cases span several 128-key tiles, several CTAs of a cluster and ragged tails; the six
 full-size workloads run in the launch configuration the benchmark times and are checked on
 sampled tokens.  Index sets are bit-exact on the integer-valued configs; elsewhere differences
 must be certified near-ties.  Attention outputs stay within max-abs 2e-2 / mean-rel 5e-3 (bf16)
