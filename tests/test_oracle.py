@@ -650,3 +650,24 @@ def test_fp8_latent_cache_page_permutation_invariance():
     sets = [[0, 3, 89, -1], [5, 149, 77, 100], [1, 2, 148, 149]]
     a, b = oracle.sfa(inp, sets), oracle.sfa(inp2, sets)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_kv8_decoding_matches_library_roundings_on_every_code():
+    """bf16(fp32(code * scale)) for all 256 codes and many scales, against numpy's float32
+    product and torch's round-to-nearest-even float32 -> bfloat16 conversion."""
+    g = np.random.default_rng(8)
+    scales = np.concatenate([g.uniform(1e-4, 3.0, 40), 2.0 ** g.integers(-20, 10, 8),
+                             [1.0 / 3.0, 0.1, 448.0 / 7.0]]).astype(np.float32)
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    fin = ~np.isnan(vals)
+    row = np.zeros(608, dtype=np.uint8)
+    for sc in scales:
+        prod = (vals[fin].astype(np.float32) * np.float32(sc)).astype(np.float32)
+        ref = torch.from_numpy(prod).to(torch.bfloat16).double().numpy()
+        row[576:580] = np.array([sc], dtype=np.float32).view(np.uint8)
+        got = []
+        for c in codes[fin]:
+            row[0] = c
+            got.append(oracle.decode_kv8(row, 0))
+        assert np.array_equal(np.array(got), ref), sc
