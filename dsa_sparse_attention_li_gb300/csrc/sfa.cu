@@ -36,6 +36,12 @@
 // With two row splits both pairs of a token form one cluster of four and merge their normalised
 // partials through distributed shared memory; with more, the partial (o, lse) go to the
 // caller's workspace and the last CTA of a (token, r) to finish merges them.
+//
+// FP8 latent cache ("Inference Optimization for Kimi K3.1 Pro", section 4: the cache stored in
+// FP8 per token and 128-column tile, the attention arithmetic in BF16): rows of 576 e4m3 codes
+// and 5 fp32 tile scales; the gather threads load codes and scales, de-quantise in registers
+// (fp32 product, bf16 rounding) and store the same swizzled BF16 tiles, so everything after the
+// gather is unchanged (template parameter KV8).
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
