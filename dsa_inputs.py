@@ -313,6 +313,37 @@ def generate(wl: Workload, device="cpu") -> dict:
     return out
 
 
+def redraw_queries(inp: dict, seed: int) -> dict:
+    """The same caches and page tables with freshly drawn query-side inputs (indexer queries
+    with their scales, head weights, attention queries), from ``seed``, by the recipes of
+    ``generate``: another decode step over the same context.  The benchmark rotates several
+    such sets so that every step selects, and gathers, other latent rows."""
+    wl = inp["wl"]
+    device = inp["q_sfa"].device
+    gv = torch.Generator(device=device).manual_seed(seed)
+    n_q = wl.n_q
+    out = dict(inp)
+    q = _draw((n_q, wl.H_I, wl.d_I), wl.values, gv, device)
+    if wl.w_values == "int14":
+        w = torch.randint(1, 5, (n_q, wl.H_I), generator=gv, device=device).to(torch.float32)
+    else:
+        w = torch.randn((n_q, wl.H_I), generator=gv, device=device) / math.sqrt(wl.H_I)
+    if wl.li_dtype == "mxfp8":
+        gm = torch.Generator(device=device).manual_seed(seed + 104729)
+        quant = (lambda x: _int_mx(x, gm)) if wl.values == "int4" else _quant_mx
+        q8, qsf = quant(q)
+        out["q_li"], out["q_sf"] = q8.contiguous(), qsf.contiguous()
+    elif wl.li_dtype == "fp8":
+        q8, qs = _quant_e4m3(q.reshape(n_q, -1), dim=1)
+        out["q_li"] = q8.view(n_q, wl.H_I, wl.d_I)
+        out["q_scale"] = qs[:, None].expand(n_q, wl.H_I).contiguous()
+    else:
+        out["q_li"] = q.to(torch.bfloat16)
+    out["w"] = w.contiguous()
+    out["q_sfa"] = _draw((n_q, wl.H, wl.d_qk), wl.values, gv, device).to(torch.bfloat16)
+    return out
+
+
 def generate_prolog(wl: Workload, device="cpu") -> dict:
     """Inputs of the Indexer Prolog for the new tokens of ``wl``: activations, random projection
     weights (the model's weights are not available; the prolog's arithmetic does not depend on

@@ -73,7 +73,8 @@ class SfaArgs(ctypes.Structure):
         "B", "n_q", "H", "d_qk", "d_v", "K", "page_size", "max_pages", "num_pages", "max_seq_len",
         "max_q_per_seq")] + [("softmax_scale", ctypes.c_float)] + [(n, ctypes.c_void_p) for n in (
             "q", "kv_pool", "page_table", "seq_lens", "q_start", "idx", "out", "lse", "status",
-            "workspace")] + [("workspace_bytes", ctypes.c_size_t), ("kv_dtype", ctypes.c_int)]
+            "workspace")] + [("workspace_bytes", ctypes.c_size_t), ("kv_dtype", ctypes.c_int),
+                             ("row_splits", ctypes.c_int)]
 
 
 _lib = None
@@ -147,9 +148,17 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def _host_max(seq_lens: torch.Tensor, q_start: torch.Tensor, max_seq_len, max_q_per_seq):
+    """The host-known bounds that size a launch.  Reading them from device tensors would be a
+    hidden device-to-host synchronisation, so a caller with device tensors must pass them."""
     if max_seq_len is None:
+        if seq_lens.is_cuda:
+            raise ValueError("max_seq_len is required with device tensors (reading it back "
+                             "would synchronise the stream)")
         max_seq_len = int(seq_lens.max())
     if max_q_per_seq is None:
+        if q_start.is_cuda:
+            raise ValueError("max_q_per_seq is required with device tensors (reading it back "
+                             "would synchronise the stream)")
         max_q_per_seq = int((q_start[1:] - q_start[:-1]).max())
     return int(max_seq_len), int(max_q_per_seq)
 
@@ -198,7 +207,7 @@ def li_topk(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_s
 
 
 def sfa_args(q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax_scale, max_seq_len=None,
-             max_q_per_seq=None, out=None, lse=None, status=None, workspace=None):
+             max_q_per_seq=None, out=None, lse=None, status=None, workspace=None, row_splits=0):
     n_q, H, d_qk = q.shape
     max_seq_len, max_q_per_seq = _host_max(seq_lens, q_start, max_seq_len, max_q_per_seq)
     a = SfaArgs()
@@ -214,13 +223,15 @@ def sfa_args(q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax_scale, m
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     # a uint8 pool holds FP8 rows (576 e4m3 codes + 5 fp32 tile scales + padding = 608 bytes)
     a.kv_dtype = DSA_FP8_E4M3 if kv_pool.dtype == torch.uint8 else DSA_BF16
+    a.row_splits = int(row_splits)
     return a
 
 
-def sfa_workspace_bytes(q, idx, **kw) -> int:
+def sfa_workspace_bytes(q, idx, row_splits=0) -> int:
     """Scratch bytes dsa_sfa_decode needs for a batch of this shape."""
     a = SfaArgs()
     a.n_q, a.H, a.K, a.d_qk, a.d_v = q.shape[0], q.shape[1], idx.shape[1], q.shape[2], 512
+    a.row_splits = int(row_splits)
     return int(load().dsa_sfa_workspace_bytes(ctypes.byref(a)))
 
 
@@ -233,7 +244,7 @@ def new_workspace(nbytes: int, device) -> Optional[torch.Tensor]:
 
 def _sfa(entry, name, q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax_scale,
          max_seq_len=None, max_q_per_seq=None, out=None, lse=None, status=None, workspace=None,
-         stream=None):
+         stream=None, row_splits=0):
     lib = load()
     n_q, H, _ = q.shape
     if out is None:
@@ -241,10 +252,10 @@ def _sfa(entry, name, q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax
     if lse is None:
         lse = torch.empty((n_q, H), dtype=torch.float32, device=q.device)
     if workspace is None and entry == "dsa_sfa_decode":
-        workspace = new_workspace(sfa_workspace_bytes(q, idx), q.device)
+        workspace = new_workspace(sfa_workspace_bytes(q, idx, row_splits), q.device)
     a = sfa_args(q, kv_pool, page_table, seq_lens, q_start, idx, softmax_scale=softmax_scale,
                  max_seq_len=max_seq_len, max_q_per_seq=max_q_per_seq, out=out, lse=lse,
-                 status=status, workspace=workspace)
+                 status=status, workspace=workspace, row_splits=row_splits)
     _check(getattr(lib, entry)(ctypes.byref(a), _stream(stream)), entry)
     return out, lse
 
@@ -256,7 +267,7 @@ def sfa_decode(q, kv_pool, page_table, seq_lens, q_start, idx, **kw):
 
 def sfa_decode_static(q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax_scale,
                       max_seq_len=None, max_q_per_seq=None, out=None, lse=None, status=None,
-                      stream=None):
+                      stream=None, row_splits=0):
     """sfa_decode for callers that cannot allocate: the split-merge scratch is the library's own
     fixed device array (SFA_STATIC_SCRATCH_BYTES, shared by every call on the device, so calls
     must not overlap on the GPU).  Only the outputs are allocated here, and only when not given."""
@@ -268,7 +279,7 @@ def sfa_decode_static(q, kv_pool, page_table, seq_lens, q_start, idx, *, softmax
         lse = torch.empty((n_q, H), dtype=torch.float32, device=q.device)
     a = sfa_args(q, kv_pool, page_table, seq_lens, q_start, idx, softmax_scale=softmax_scale,
                  max_seq_len=max_seq_len, max_q_per_seq=max_q_per_seq, out=out, lse=lse,
-                 status=status, workspace=None)
+                 status=status, workspace=None, row_splits=row_splits)
     _check(lib.dsa_sfa_decode_static(ctypes.byref(a), _stream(stream)), "dsa_sfa_decode_static")
     return out, lse
 
@@ -376,7 +387,8 @@ def indexer_prolog(inp: dict, *, q_out=None, q_sf=None, w_out=None, workspace=No
 
 
 def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=None, status=None,
-                stream=None, max_seq_len=None, max_q_per_seq=None, prefill: bool = False):
+                stream=None, max_seq_len=None, max_q_per_seq=None, prefill: bool = False,
+                row_splits: int = 0):
     """One pass of the whole hot path over a batch laid out as ``dsa_inputs.generate`` does:
     li_topk followed by sfa_decode (or sfa_prefill) on the same stream."""
     wl = inp["wl"]
@@ -390,5 +402,6 @@ def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=
     kv = inp["kv8_pool"] if getattr(wl, "kv_dtype", "bf16") == "fp8" else inp["kv_pool"]
     out, lse = f(inp["q_sfa"], kv, inp["pt_kv"], inp["seq_lens"], inp["q_start"], idx,
                  softmax_scale=inp["softmax_scale"], max_seq_len=ms, max_q_per_seq=mq, out=out,
-                 lse=lse, status=status, workspace=workspace, stream=stream)
+                 lse=lse, status=status, workspace=workspace, stream=stream,
+                 row_splits=row_splits)
     return idx, cnt, out, lse

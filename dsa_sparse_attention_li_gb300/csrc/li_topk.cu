@@ -63,8 +63,6 @@ struct Params {
   int* out_idx;
   int* out_cnt;
   int* status;
-  const void* q;       // raw pointers (used by the CUDA-core scoring variant only)
-  const void* k_pool;
   const uint8_t* q_sf;  // MXFP8: E8M0 scales of 32-element groups, [n_q][H_I][D_I/32]
   const uint8_t* k_sf;  //        and [num_pages][64][D_I/32]
   float* out_score;     // optional [n_q][K]: the score of every emitted position (-inf padding)
@@ -233,17 +231,9 @@ DSA_DEV void find_bin_local(const uint32_t* h, uint32_t need, int tt, CtlT* ctl)
   __syncthreads();
 }
 
-DSA_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-DSA_DEV float e4m3_to_float(uint8_t b) {
-  __nv_fp8_e4m3 v;
-  v.__x = b;
-  return float(v);
-}
-
 // ---- the fused kernel ----
 
-template <int D_I, bool FP8, int H_I, int T, bool kTensorCore, bool MX>
+template <int D_I, bool FP8, int H_I, int T, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     li_topk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const Params p) {
@@ -302,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     fence_barrier_init();
   }
-  if (kTensorCore && warp == 1) {
+  if (warp == 1) {
     tmem_alloc(&ctl->tmem_base, CF::kTmemCols);
     tmem_relinquish();
   }
@@ -335,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &ctl->abort;
 
   // ---------------- streaming phase: scores of [lo, lo + nscan) into shared memory
-  if constexpr (kTensorCore) {
+  {
     const uint32_t tmem = ctl->tmem_base;
     if (warp == 0 && lane == 0 && ntile > 0) {
       prefetch_tmap(&tm_k);
@@ -498,47 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->tempty[a]);
       }
     }
-  } else {
-    // CUDA-core scoring (debug variant of the same kernel: identical select phase)
-    for (int e = tid; e < nscan; e += kThreads) {
-      const int j = lo + e;
-      const int pg = pages[e >> 6];
-      const size_t row = (size_t)(pg < 0 ? 0 : pg) * 64 + (j & 63);
-      float ks = 1.f;
-      if (FP8 && !MX) ks = p.k_scale[row];
-      for (int tt = 0; tt < T; ++tt) {
-        float s = 0.f;
-        for (int h = 0; tt < nt && h < H_I; ++h) {  // tokens of the group only (t0 + tt < n_q)
-          float dot = 0.f;
-          for (int d = 0; d < D_I; ++d) {
-            float qv, kv;
-            if (FP8) {
-              qv = e4m3_to_float(((const uint8_t*)p.q)[((size_t)(t0 + tt) * H_I + h) * D_I + d]);
-              kv = e4m3_to_float(((const uint8_t*)p.k_pool)[row * D_I + d]);
-              if (MX) {
-                qv = ldexpf(qv, (int)p.q_sf[((size_t)(t0 + tt) * H_I + h) * (D_I / 32) + d / 32] - 127);
-                kv = ldexpf(kv, (int)p.k_sf[row * (D_I / 32) + d / 32] - 127);
-              }
-            } else {
-              qv = bf16_bits_to_float(((const uint16_t*)p.q)[((size_t)(t0 + tt) * H_I + h) * D_I + d]);
-              kv = bf16_bits_to_float(((const uint16_t*)p.k_pool)[row * D_I + d]);
-            }
-            dot = fmaf(qv, kv, dot);
-          }
-          s = fmaf(wts[tt * H_I + h], fmaxf(dot, 0.f), s);
-        }
-        if (FP8 && !MX) s *= ks;
-        const bool valid = tt < nt && pg >= 0 && j <= pos0 + tt;
-        const uint32_t u = valid ? score_key(s) : 0u;
-        scores[tt * p.chunk + e] = u;
-        if (valid) atomicAdd(&hist[tt * kHistWords + (u >> 22)], 1u << (((u >> 21) & 1u) * 16u));
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (kTensorCore && warp == 1) {
+  if (warp == 1) {
     __syncwarp();
     tmem_dealloc(ctl->tmem_base, CF::kTmemCols);
   }
@@ -1119,11 +1073,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-static bool use_cuda_core_scores() {
-  const char* e = std::getenv("DSA_LI_CUDA_CORE_SCORES");
-  return e && e[0] == '1';
-}
-
 template <int D_I, bool FP8, int H_I, int T, bool MX = false>
 static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::string& err) {
   using CF = Cfg<D_I, FP8, H_I, T, MX>;
@@ -1132,8 +1081,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   const int groups = (a.max_q_per_seq + T - 1) / T;
   const int maxL = std::max(a.max_seq_len, 1);
 
-  const bool simple = use_cuda_core_scores();
-  auto kern = simple ? li_topk_kernel<D_I, FP8, H_I, T, false, MX> : li_topk_kernel<D_I, FP8, H_I, T, true, MX>;
+  auto kern = li_topk_kernel<D_I, FP8, H_I, T, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: set shared memory size", err);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1145,10 +1093,8 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   // select phase (which scans each CTA's chunk and does not overlap the stream).
   struct Choice { int ns, c, chunk, smem; };
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int, int>, Choice> memo;
-  const int forced_c = std::getenv("DSA_LI_CLUSTER") ? std::atoi(std::getenv("DSA_LI_CLUSTER")) : 0;
-  const int forced_ns = std::getenv("DSA_LI_STAGES") ? std::atoi(std::getenv("DSA_LI_STAGES")) : 0;
-  const auto key = std::make_tuple(dev.device, maxL, a.B * groups, forced_c, forced_ns);
+  static std::map<std::tuple<int, int, int>, Choice> memo;
+  const auto key = std::make_tuple(dev.device, maxL, a.B * groups);
   Choice best{0, 0, 0, 0};
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -1159,9 +1105,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
     double best_est = 1e300;
     const long long clusters = (long long)a.B * groups;
     for (int ns = 8; ns >= 2; --ns) {
-      if (forced_ns && ns != forced_ns) continue;
       for (int c = 1; c <= kMaxCluster; ++c) {
-        if (forced_c && c != forced_c) continue;
         const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
         if (chunk > 65535 || (long long)chunk * c < maxL) continue;
         const Layout lay(ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
@@ -1235,8 +1179,6 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.out_idx = a.out_idx;
   p.out_cnt = a.out_cnt;
   p.status = a.status;
-  p.q = a.q;
-  p.k_pool = a.k_pool;
   p.q_sf = a.q_sf;
   p.k_sf = a.k_sf;
   p.out_score = a.out_score;
@@ -1253,9 +1195,6 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (std::getenv("DSA_VERBOSE"))
-    std::fprintf(stderr, "[dsa] li_topk D_I=%d fp8=%d H_I=%d T=%d cluster=%d chunk=%d stages=%d smem=%d grid=%u\n",
-                 D_I, (int)FP8, H_I, T, best_c, best_chunk, best_ns, best_smem, cfg.gridDim.x);
   e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_q, p);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: launch", err);
   return DSA_OK;

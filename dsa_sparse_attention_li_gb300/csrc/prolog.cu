@@ -492,10 +492,6 @@ dsa_status launch_prolog(const dsa_prolog_args& a, cudaStream_t stream, std::str
   cudaError_t e = cudaFuncSetAttribute(prolog_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return cuda_fail(e, "indexer_prolog: set shared memory size", err);
   const unsigned grid = (unsigned)(pl.ctas_q + 2 * pl.ctas_k);
-  if (std::getenv("DSA_VERBOSE"))
-    std::fprintf(stderr, "[dsa] prolog ntok q=%d kw=%d tiles q=%d kw=%d splits q=%d kw=%d (chunks %d/%d) grid=%u smem=%d ws=%zu\n",
-                 pl.ntok_q, pl.ntok_kw, pl.tiles_q, pl.tiles_kw, pl.splits_q, pl.splits_kw, pl.per_q, pl.per_kw,
-                 grid, pl.smem, pl.ws_bytes);
   prolog_kernel<<<grid, kThreads, pl.smem, stream>>>(tm_wq, tm_wk, tm_ww, tm_xq, tm_x, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "indexer_prolog: launch", err);

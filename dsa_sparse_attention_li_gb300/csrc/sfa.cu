@@ -826,59 +826,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// CUDA-core variant (debug aid, selected by DSA_SFA_CUDA_CORE=1): one CTA per (token, head),
-// direct two-pass softmax over the index set.
-__global__ void __launch_bounds__(128) sfa_cuda_core_kernel(const Params p) {
-  __shared__ float z[kMaxRows];
-  __shared__ float red[4];
-  const int t = blockIdx.x / p.H, h = blockIdx.x % p.H, tid = threadIdx.x;
-  const int b = find_seq(p.q_start, p.B, t);
-  const int L = min(p.seq_lens[b], p.max_pages * 64);  // positions the page table covers
-  const __nv_bfloat16* qh = p.q + ((size_t)t * p.H + h) * kDqk;
-  float m = -INFINITY;
-  for (int r = tid; r < p.K; r += 128) {
-    const int j = p.idx[(size_t)t * p.K + r];
-    float v = -INFINITY;
-    if (j >= 0 && j < L) {
-      const int pg = p.page_table[(size_t)b * p.max_pages + (j >> 6)];
-      if (pg >= 0 && pg < p.num_pages) {
-        const __nv_bfloat16* kv = p.kv + ((size_t)pg * 64 + (j & 63)) * kDqk;
-        float d = 0.f;
-        for (int c = 0; c < kDqk; ++c) d = fmaf(__bfloat162float(qh[c]), __bfloat162float(kv[c]), d);
-        v = d * p.scale_log2;
-      }
-    }
-    z[r] = v;
-    m = fmaxf(m, v);
-  }
-  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((tid & 31) == 0) red[tid >> 5] = m;
-  __syncthreads();
-  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float l = 0.f;
-  for (int r = tid; r < p.K; r += 128) {
-    const float e = (m == -INFINITY || z[r] == -INFINITY) ? 0.f : exp2f(z[r] - m);
-    z[r] = e;
-    l += e;
-  }
-  for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  if ((tid & 31) == 0) red[tid >> 5] = l;
-  __syncthreads();
-  l = red[0] + red[1] + red[2] + red[3];
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int r = 0; r < p.K; ++r) {
-    if (z[r] == 0.f) continue;
-    const int j = p.idx[(size_t)t * p.K + r];
-    const int pg = p.page_table[(size_t)b * p.max_pages + (j >> 6)];
-    const __nv_bfloat16* kv = p.kv + ((size_t)pg * 64 + (j & 63)) * kDqk;
-    for (int k = 0; k < 4; ++k) acc[k] = fmaf(z[r], __bfloat162float(kv[tid * 4 + k]), acc[k]);
-  }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  for (int k = 0; k < 4; ++k) p.out[((size_t)t * p.H + h) * kDv + tid * 4 + k] = __float2bfloat16(acc[k] * inv);
-  if (tid == 0 && p.lse) p.lse[(size_t)t * p.H + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-}
-
 // ---------------------------------------------------------------- host side
 
 struct Plan {
@@ -895,10 +842,7 @@ static Plan plan(const dsa_sfa_args& a, bool prefill, int sm_count) {
     // never more than the CTAs one wave holds
     while (splits > 1 && 2LL * a.n_q * splits > sm_count) --splits;
   }
-  if (const char* e = std::getenv("DSA_SFA_SPLITS")) {
-    const int s = std::atoi(e);
-    if (s >= 1 && s <= 64) splits = s;
-  }
+  if (!prefill && a.row_splits > 0) splits = std::min(a.row_splits, (a.K + kNT - 1) / kNT);
   int rows_per = ((a.K + splits - 1) / splits + kNT - 1) / kNT * kNT;
   while (rows_per > kMaxRows) {  // K up to 2048 always fits one split
     ++splits;
@@ -976,16 +920,6 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   if (a.n_q == 0) return DSA_OK;
 
   const bool kv8 = a.kv_dtype == DSA_FP8_E4M3;
-  const char* simple = std::getenv("DSA_SFA_CUDA_CORE");
-  if (simple && simple[0] == '1') {
-    if (kv8) {
-      err = "sfa (cuda-core): bf16 latent cache only";
-      return DSA_ERR_UNSUPPORTED;
-    }
-    sfa_cuda_core_kernel<<<a.n_q * a.H, 128, 0, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "sfa (cuda-core): launch", err);
-  }
 
   CUtensorMap tm_q, tm_qr;
   if (!encode_tmap_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kDqk, (uint64_t)a.n_q * a.H,
@@ -999,10 +933,6 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "sfa: set shared memory size", err);
   const unsigned grid = (unsigned)(a.n_q * 2 * pl.splits);
-  if (std::getenv("DSA_VERBOSE"))
-    std::fprintf(stderr, "[dsa] sfa %s splits=%d rows_per=%d cluster_merge=%d grid=%u smem=%d\n",
-                 prefill ? "prefill" : "decode", pl.splits, pl.rows_per, (int)pl.cluster_merge, grid,
-                 smem);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 5
+#define DSA_ABI_VERSION 6
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -172,6 +172,9 @@ typedef struct {
   void* workspace;           /* device scratch of dsa_sfa_workspace_bytes(), 256-B aligned */
   size_t workspace_bytes;
   dsa_dtype kv_dtype;        /* DSA_BF16 (rows of 576 bf16) or DSA_FP8_E4M3 (608-byte rows) */
+  int row_splits;            /* dsa_sfa_decode: CTA pairs that share one token's K rows
+                                (0 = chosen from the SM count; the result does not depend on
+                                it beyond fp32 rounding); ignored by dsa_sfa_prefill        */
 } dsa_sfa_args;
 
 /* Scratch that dsa_sfa_decode needs for these arguments (0 if none).  Host only, no CUDA. */
@@ -292,12 +295,23 @@ dsa_status dsa_indexer_prolog(const dsa_prolog_args* args, dsa_stream_t stream);
 /* Cache layout and page-table helpers                                                         */
 /* ------------------------------------------------------------------------------------------ */
 
+/*
+ * The caches are paged: the indexer reads the paged key cache directly ("Day0 Inference
+ * Adaptation for Next-Gen LLMs ... CANN", section 3.1), and the selected indices address the
+ * paged KV cache page by page ("Inference Optimization for Kimi K3.1 Pro", section 2, "Inlined
+ * Top-K Selection": on-demand in-page addressing).  The helpers below describe and maintain
+ * that layout; they are host-side conveniences (the pages define no interface).
+ */
+
 /* Bytes of one page of `rows` rows of `dim` elements of `dtype` (0 on invalid input); for
- * MXFP8 the elements only (the E8M0 scales are a separate [rows][dim/32] byte array). */
+ * MXFP8 the elements only (the E8M0 scales are a separate [rows][dim/32] byte array, the
+ * group-32 scales of "Inference Optimization for Kimi K3.1 Pro", section 4). */
 size_t dsa_page_bytes(dsa_dtype dtype, int rows, int dim);
 
 /*
- * Host-side check of a page table (host pointers): for every sequence b, the pages
+ * Host-side check of a page table (host pointers) before it drives the in-page addressing of
+ * the kernels ("Inference Optimization for Kimi K3.1 Pro", section 2, "Inlined Top-K
+ * Selection"): for every sequence b, the pages
  * 0 .. ceil(seq_lens[b]/page_size)-1 hold ids in [0, num_pages), and (if require_unique) no id
  * is used twice over the whole table.  Entries past a sequence's last page are ignored.
  * Returns DSA_OK or DSA_ERR_INVALID_ARG (reason in dsa_last_error()).
@@ -307,7 +321,11 @@ dsa_status dsa_page_table_validate(const int32_t* page_table_host, int B, int ma
                                    int require_unique);
 
 /*
- * Scatter n_rows new cache rows into a paged pool (device pointers):
+ * Append new rows to a paged cache: the write of the new tokens' keys that the indexer's input
+ * preparation performs ("Inference Optimization for Kimi K3.1 Pro", section 3, "Three-Stream
+ * Parallel Architecture", the K normalisation stream; dsa_indexer_prolog does this itself for
+ * the key cache), or of latent rows for the attention cache.  Scatter n_rows rows (device
+ * pointers):
  *   pool[page_table[seq[r]][pos[r] / page_size]][pos[r] % page_size][:] = rows[r][:]
  * and, when row_scales is not NULL, scale_pool[same page][same slot] = row_scales[r] (the
  * per-row fp32 scale of an FP8 key cache).  elem_bytes is 2 (bf16) or 1 (e4m3); dim*elem_bytes

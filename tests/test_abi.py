@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     lib = dsa.load()
-    assert lib.dsa_abi_version() == 5
+    assert lib.dsa_abi_version() == 6
     assert dsa.status_string(0) == "DSA_OK"
     assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
     assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"

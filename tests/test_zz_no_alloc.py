@@ -10,8 +10,6 @@ It also checks that arguments needing more scratch than the fixed capacity are r
 
 Kept in its own file, named to be collected last.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -58,17 +56,10 @@ def test_static_scratch_decode_matches_workspace_decode(cuda_lib):
 
 def test_static_scratch_rejects_arguments_beyond_capacity(cuda_lib):
     wl, inp, idx = _inputs()
-    old = os.environ.get("DSA_SFA_SPLITS")
-    os.environ["DSA_SFA_SPLITS"] = "32"  # 4 tokens x 2 halves x 32 splits of partials > capacity
-    try:
-        assert dsa.sfa_workspace_bytes(inp["q_sfa"], idx) > dsa.SFA_STATIC_SCRATCH_BYTES
-        with pytest.raises(dsa.DsaError) as e:
-            dsa.sfa_decode_static(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"],
-                                  inp["q_start"], idx, **_kw(wl, inp))
-        assert e.value.code == dsa.DSA_ERR_UNSUPPORTED
-        assert "capacity" in str(e.value)
-    finally:
-        if old is None:
-            del os.environ["DSA_SFA_SPLITS"]
-        else:
-            os.environ["DSA_SFA_SPLITS"] = old
+    # 4 tokens x 2 halves x 32 splits of partials exceed the fixed capacity
+    assert dsa.sfa_workspace_bytes(inp["q_sfa"], idx, row_splits=32) > dsa.SFA_STATIC_SCRATCH_BYTES
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.sfa_decode_static(inp["q_sfa"], inp["kv_pool"], inp["pt_kv"], inp["seq_lens"],
+                              inp["q_start"], idx, row_splits=32, **_kw(wl, inp))
+    assert e.value.code == dsa.DSA_ERR_UNSUPPORTED
+    assert "capacity" in str(e.value)
