@@ -25,6 +25,7 @@ from . import build as _build
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa.so")
+HOOKS_LIB_PATH = os.path.join(_PKG, "libdsa_testhooks.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK, DSA_ERR_TIMEOUT = range(6)
 DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
@@ -78,6 +79,7 @@ class SfaArgs(ctypes.Structure):
 
 
 _lib = None
+_hooks = None
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
@@ -89,7 +91,28 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         _build.build()
     if not os.path.exists(LIB_PATH):
         raise RuntimeError("libdsa.so not built (run __graft_entry__.build())")
-    lib = ctypes.CDLL(LIB_PATH)
+    _lib = _configure(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def load_testhooks(build_if_missing: bool = True) -> ctypes.CDLL:
+    """The test build libdsa_testhooks.so (short device-side wait limits and
+    dsa_test_inject_stall; include/dsa_testhooks.h).  For the failure-handling tests only."""
+    global _hooks
+    if _hooks is not None:
+        return _hooks
+    if build_if_missing and not _build.up_to_date(HOOKS_LIB_PATH):
+        _build.build(hooks=True)
+    if not os.path.exists(HOOKS_LIB_PATH):
+        raise RuntimeError("libdsa_testhooks.so not built (run __graft_entry__.build())")
+    lib = _configure(ctypes.CDLL(HOOKS_LIB_PATH))
+    lib.dsa_test_inject_stall.argtypes = [ctypes.c_int]
+    lib.dsa_test_inject_stall.restype = None
+    _hooks = lib
+    return lib
+
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     P = ctypes.c_void_p
     lib.dsa_status_string.argtypes = [ctypes.c_int]
     lib.dsa_status_string.restype = ctypes.c_char_p
@@ -116,7 +139,6 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.dsa_cache_write.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     P, ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_int, P, P]
     lib.dsa_cache_write.restype = ctypes.c_int
-    _lib = lib
     return lib
 
 

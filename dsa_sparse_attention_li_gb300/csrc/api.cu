@@ -25,6 +25,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 namespace dsa {
 
+#ifdef DSA_TEST_HOOKS
+int g_test_stall = 0;
+#endif
+
 void set_last_error(const std::string& why) { g_last_error = why; }
 
 bool device_info(DeviceInfo& info, std::string& err) {
@@ -294,5 +298,10 @@ dsa_status dsa_cache_write(void* pool, float* scale_pool, int num_pages, int pag
   if (s != DSA_OK) g_last_error = err;
   return s;
 }
+
+#ifdef DSA_TEST_HOOKS
+// Test build only (libdsa_testhooks.so; include/dsa_testhooks.h).
+void dsa_test_inject_stall(int kernel) { dsa::g_test_stall = kernel; }
+#endif
 
 }  // extern "C"

@@ -28,6 +28,12 @@ bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* bas
                     uint64_t inner, uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
                     uint32_t box_outer, CUtensorMapSwizzle swizzle, std::string& err);
 
+#ifdef DSA_TEST_HOOKS
+// Test build only: which kernel's first CTA makes one of its waits wait on a barrier that nothing
+// arrives on (0 none, 1 li_topk, 2 sparse attention); set by dsa_test_inject_stall().
+extern int g_test_stall;
+#endif
+
 // Sets the calling thread's dsa_last_error() text.
 void set_last_error(const std::string& why);
 

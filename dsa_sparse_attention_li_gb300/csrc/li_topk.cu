@@ -66,6 +66,9 @@ struct Params {
   const uint8_t* q_sf;  // MXFP8: E8M0 scales of 32-element groups, [n_q][H_I][D_I/32]
   const uint8_t* k_sf;  //        and [num_pages][64][D_I/32]
   float* out_score;     // optional [n_q][K]: the score of every emitted position (-inf padding)
+#ifdef DSA_TEST_HOOKS
+  int stall;            // test build: CTA 0's MMA thread waits on a barrier nothing arrives on
+#endif
 };
 
 template <int D_I, bool FP8, int H_I, int T, bool MX = false>
@@ -118,6 +121,9 @@ struct Ctl {
   uint64_t qbar;
   uint64_t drain;
   uint64_t sinit;  // MXFP8: the first scale cells are in tensor memory
+#ifdef DSA_TEST_HOOKS
+  uint64_t never;  // test build: no thread ever arrives here
+#endif
   uint32_t tmem_base;
   int abort;
   uint32_t scan[kThreads / 32];
@@ -289,6 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->qbar, 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->sinit, 256);  // both epilogue groups
+#ifdef DSA_TEST_HOOKS
+    mbar_init(&ctl->never, 1);
+#endif
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -338,10 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with the evict-first L2 policy.  Otherwise other groups re-read it from L2.
       const bool read_once = p.groups == 1;
       const uint64_t pol = l2_policy_evict_first();
+      int issued = 0;
       for (int i = 0; i < ntile; ++i) {
         const int s = i % p.nstage;
         const uint32_t ph = (uint32_t)(i / p.nstage) & 1u;
         if (i >= p.nstage && !mbar_wait(&ctl->empty[s], ph ^ 1u, abort, p.status)) break;
+        issued = i + 1;
         const int pg0 = pages[2 * i], pg1 = pages[2 * i + 1];
         const uint32_t bytes = (uint32_t)((pg0 >= 0) + (pg1 >= 0)) * CF::kBoxes * 64 * 128;
         mbar_arrive_expect_tx(&ctl->full[s], bytes);
@@ -358,10 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // never leave with copies in flight: wait for the last fill of every stage
-      for (int i = max(0, ntile - p.nstage); i < ntile; ++i) {
+      // never leave with copies in flight: wait for the last fill of every stage issued (also
+      // after an abort: the ring is reused by the select phase)
+      for (int i = max(0, issued - p.nstage); i < issued; ++i) {
         const int s = i % p.nstage;
-        mbar_wait(&ctl->full[s], (uint32_t)(i / p.nstage) & 1u, abort, p.status);
+        mbar_wait_drain(&ctl->full[s], (uint32_t)(i / p.nstage) & 1u, p.status);
       }
     } else if (warp == 1 && lane == 0 && ntile > 0) {
       constexpr uint32_t idesc =
@@ -369,6 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(q_s);
       const uint32_t st_addr = smem_u32(stage_base);
       bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
+#ifdef DSA_TEST_HOOKS
+      if (p.stall == 1 && blockIdx.x == 0) ok = ok && mbar_wait(&ctl->never, 0, abort, p.status);
+#endif
       if constexpr (MX) ok = ok && mbar_wait(&ctl->sinit, 0, abort, p.status);
       for (int i = 0; ok && i < ntile; ++i) {
         const int s = i % p.nstage;
@@ -495,6 +510,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(ctl->tmem_base, CF::kTmemCols);
+  }
+  if (*abort) {
+    // A wait of this CTA gave up (DSA_ERR_TIMEOUT is in *status): keys of tiles it did not
+    // reduce were never written.  The select still runs -- every CTA of the cluster takes the
+    // same cluster barriers -- over no keys of this CTA, so that every shared-memory index it
+    // derives stays in bounds; the token's output is unspecified.
+    for (int i = tid; i < T * p.chunk; i += kThreads) scores[i] = 0u;
+    for (int i = tid; i < T * kHistWords; i += kThreads) hist[i] = 0u;
+    __syncthreads();
   }
 
   // The next kernel in the stream (sparse attention) may begin its prologue on idle SMs; it reads
@@ -1182,6 +1206,9 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.q_sf = a.q_sf;
   p.k_sf = a.k_sf;
   p.out_score = a.out_score;
+#ifdef DSA_TEST_HOOKS
+  p.stall = g_test_stall;
+#endif
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(best_c * a.B * groups));

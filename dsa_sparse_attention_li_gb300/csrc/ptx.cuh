@@ -16,7 +16,13 @@
 
 namespace dsa {
 
+#ifdef DSA_TEST_HOOKS
+// Test build (libdsa_testhooks.so): a short limit, so that a test can make a wait run out
+// quickly and check that the kernel reports it and frees what it holds.
+constexpr uint64_t kWaitLimitNs = 20ull * 1000ull * 1000ull;    // 20 ms per wait
+#else
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s per wait
+#endif
 constexpr uint32_t kSuspendHintNs = 20000u;                       // sleep per try_wait
 
 enum : int { kStatusOk = 0, kStatusDeviceCheck = 4, kStatusTimeout = 5 };
@@ -152,6 +158,21 @@ DSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int*
       return false;
     }
   }
+}
+
+// Bounded wait that does not give up when the CTA has aborted: for draining asynchronous copies
+// that were issued and will complete (their bytes exist) before their destination is reused or
+// the CTA exits.
+DSA_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      report(status, kStatusTimeout);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -103,6 +103,9 @@ struct Params {
   int* ws_count;   // [n_q][2] arrival counters (zero between calls)
   const __nv_bfloat16* q;
   const __nv_bfloat16* kv;
+#ifdef DSA_TEST_HOOKS
+  int stall;       // test build: CTA 0's MMA thread waits on a barrier nothing arrives on
+#endif
 };
 
 // Shared memory.  The TMA-staged value columns of Q[:, D_r] (4 boxes of 128 heads x 128 B) are
@@ -133,6 +136,9 @@ struct Ctl {
   int nvalid;
   int gather_go[2];  // poller's verdict per step (read by all gather threads after bar.sync)
   uint64_t mrg;      // cluster merge: the other split's rows and lse have arrived
+#ifdef DSA_TEST_HOOKS
+  uint64_t never;    // test build: no thread ever arrives here
+#endif
 };
 
 DSA_DEV int find_seq(const int* q_start, int B, int t) {
@@ -235,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->xfree[x], 128);
     }
     mbar_init(&ctl->mrg, 1);
+#ifdef DSA_TEST_HOOKS
+    mbar_init(&ctl->never, 1);
+#endif
     ctl->abort = 0;
     ctl->nvalid = 0;
     fence_barrier_init();
@@ -404,6 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t rope_desc = sdesc_sw64(smem_u32(st_s) + 4u * kBoxBytes, 512);
     const uint64_t p_desc = sdesc_sw128(smem_u32(smem + Layout::pbuf), 16, 1024);
     bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
+#ifdef DSA_TEST_HOOKS
+    if (p.stall == 2 && blockIdx.x == 0) ok = ok && mbar_wait(&ctl->never, 0, abort, p.status);
+#endif
     ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
     // Issue whichever is ready: P.V of the oldest tile whose weights are written (needs P; it
     // releases a ring stage) is tested first, then Q.K^T of the next tile (needs its rows and a
@@ -905,6 +917,9 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
   p.status = a.status;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.kv = reinterpret_cast<const __nv_bfloat16*>(a.kv_pool);
+#ifdef DSA_TEST_HOOKS
+  p.stall = g_test_stall;
+#endif
   if (need > 0) {
     const size_t units = (size_t)a.n_q * 2 * pl.splits;
     uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);

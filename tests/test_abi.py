@@ -182,3 +182,12 @@ def test_topk_merge_host_validation():
     assert lib.dsa_topk_merge(ctypes.byref(a), None) == dsa.DSA_ERR_INVALID_ARG
     a.n_q = 0
     assert lib.dsa_topk_merge(ctypes.byref(a), None) == dsa.DSA_OK  # nothing to merge
+
+
+def test_test_hook_symbol_only_in_the_test_build():
+    """dsa_test_inject_stall (include/dsa_testhooks.h) exists in libdsa_testhooks.so only."""
+    assert not hasattr(dsa.load(), "dsa_test_inject_stall")
+    hooks = dsa.load_testhooks()
+    assert hasattr(hooks, "dsa_test_inject_stall")
+    for n in dsa.SYMBOLS:
+        assert hasattr(hooks, n), n
