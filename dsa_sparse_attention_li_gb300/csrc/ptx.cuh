@@ -107,6 +107,19 @@ DSA_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity` with acquire semantics at cluster scope (for phases completed
+// by another CTA's asynchronous stores).
+DSA_DEV bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try_wait, with acquire semantics at cluster scope: for phases completed by arrivals
 // of another CTA of the cluster that released its own shared::cluster stores.
 DSA_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -136,6 +149,15 @@ DSA_DEV void st_async_v4(uint32_t cluster_addr, uint4 v, uint32_t remote_bar) {
           cluster_addr),
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
       : "memory");
+}
+
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster, counted (4 bytes) on
+// that CTA's mbarrier `remote_bar`.
+DSA_DEV void st_async_b32(uint32_t cluster_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   cluster_addr),
+               "r"(v), "r"(remote_bar)
+               : "memory");
 }
 
 // Bounded wait for phase `parity` of `bar`.  Returns false (and raises *abort) when the limit
@@ -219,6 +241,20 @@ DSA_DEV void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, 
 // Named barrier over `nthreads` threads (a multiple of 32); blocks in hardware.
 DSA_DEV void named_barrier(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also reduces a predicate: every participating thread gets the AND of `v`
+// over all of them, so a group can decide together (e.g. to leave a loop) and never strand a
+// member at a later barrier.
+DSA_DEV bool named_barrier_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 DSA_DEV void fence_proxy_async_smem() {

@@ -22,14 +22,22 @@
 //     zero-filled) into a 4-stage ring (value boxes [box][row][128 B] with the 128-byte swizzle,
 //     rope box with 64-byte rows), so a stage is the K-major B operand of Q.K^T (N = 64 rows)
 //     and its value boxes the MN-major B operand of P.V (K = 64 rows, N = 256);
-//   - S_r = Q[:, D_r].K[:, D_r]^T goes to one of two TMEM buffers; four exchange warps send S_r
+//   - S_r = Q[:, D_r].K[:, D_r]^T goes to one of two TMEM buffers.  The pair splits each tile's
+//     columns for the softmax: CTA r finalises columns [32r, 32r + 32) for all 128 heads, so
+//     the exponentials of every head row spread over the four TMEM lane quadrants (each served
+//     by its own SM sub-partition).  Eight score warps form two teams that take alternate
+//     tiles, one thread per head row: a thread sends the CTA's partial of the peer's columns
 //     to the peer through distributed shared memory (asynchronous stores counted on the peer's
-//     mbarrier), add the peer's partial in the same order in both CTAs (S_0 + S_1), mask and
-//     scale it and take the row maximum, one tile ahead of the softmax;
-//   - one softmax thread per head (TMEM lane) exponentiates its row, writes P (bf16) into one of
-//     two shared-memory buffers (A operand of P.V) and accumulates the row sums in fp32; the
-//     reference maximum only moves when a tile's maximum exceeds it by more than 2^8, and only
-//     then is the head's O row rescaled in TMEM;
+//     mbarrier), adds the peer's partial of its own columns (always S_0 + S_1), masks and
+//     scales them, exchanges its row maximum with the peer (512 bytes a tile; both CTAs then
+//     hold the same maximum and take the same rescale decisions), takes the reference maximum
+//     the other team left after the previous tile, exponentiates and writes its columns of P
+//     (bf16) into its P buffer and the peer's (the A operand of P.V in both).  Distributed
+//     shared memory moves about 20 bytes per clock, so the tile moves 16 KiB of partial scores
+//     and 8 KiB of P each way instead of both full partials (32 KiB); and with two teams one
+//     tile's round trips to the peer overlap the next tile's.  The reference maximum only
+//     moves when a tile's maximum exceeds it by more than 2^8; then each CTA rescales its O
+//     rows;
 //   - O (128 x 256 fp32 = half of TMEM) accumulates P.V_r across tiles.
 // Each head's 128x512 fp32 O would fill all of TMEM, hence the value split over the pair; the
 // split of the Q.K^T dimensions halves both the gathered bytes and the tensor work of each CTA.
@@ -53,21 +61,15 @@
 namespace dsa {
 namespace sfa {
 
-constexpr int kThreads = 512;  // 16 warps: 0-3, 9-11 gather; 4-7 score exchange; 8 MMA; 12-15 softmax
+constexpr int kThreads = 512;  // 16 warps: 0-3, 9-11 gather; 8 MMA; 4-7 and 12-15 score warps
 constexpr int kGatherThreads = 224;
-constexpr int kXchgWarp0 = 4;
 constexpr int kMmaWarp = 8;
-constexpr int kSoftmaxWarp0 = 12;
 constexpr int kHeads = 128;        // MMA M (heads are padded to 128)
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kDvHalf = 256;
 constexpr int kNT = 64;            // gathered rows per tile (MMA N of Q.K^T)
 constexpr int kStages = 4;
-constexpr int kXBufs = 1;          // partial-S exchange buffers
-// Q[:, D_r] value columns are staged (64 KiB) in the exchange buffers when they are large
-// enough, else in the last two ring stages (whose first gathers then wait for Q to reach TMEM)
-constexpr bool kQInRing = kXBufs * 32768 < 65536;
 constexpr int kBoxBytes = kNT * 128;                        // one value box of a tile: 8 KiB
 constexpr int kRopeHalf = 32;      // rope columns of this CTA's half of Q.K^T
 constexpr int kRopeBoxBytes = kNT * kRopeHalf * 2;          // 64-byte rows: 4 KiB
@@ -76,6 +78,12 @@ constexpr int kRowChunks = 32 + 4;                          // 16-byte chunks ga
 constexpr int kChunks = kNT * kRowChunks;                   // per tile (2304)
 constexpr int kMaxRows = 2048;     // row slots per CTA
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kFinCols = kNT / 2;  // columns of a tile whose softmax this CTA finalises
+// bytes that arrive per tile through distributed shared memory
+constexpr uint32_t kXBytes = kHeads * kFinCols * 4;         // the peer's partial S of our columns
+constexpr uint32_t kMxBytes = kHeads * 4;                   // the peer's row maxima of its columns
+constexpr uint32_t kPRemBytes = kHeads * kFinCols * 2;      // the peer's columns of P (bf16)
+constexpr uint32_t kFinBytes = kHeads * 8;                  // the peer's partial row sums
 // TMEM columns (512 in total)
 constexpr uint32_t kColQ = 0;      // Q value columns of D_r: 256 bf16 per lane = 128 columns
 constexpr uint32_t kColS = 128;    // partial S, two buffers of 64 columns (tile i uses i & 1)
@@ -88,8 +96,8 @@ struct Params {
   int B, n_q, H, K, max_pages, num_pages;
   int splits;      // row splits per token
   int rows_per;    // row slots per split (multiple of kNT)
-  int cluster_merge;  // splits == 2: the two splits of a token share a cluster of 4 and merge
-                      // through distributed shared memory (no workspace)
+  int cluster_merge;  // splits == 2: the two splits of a token share a cluster of 4 and each
+                      // finalises half of the heads (rows exchanged through the workspace)
   float scale_log2;  // softmax_scale * log2(e)
   const int* page_table;
   const int* seq_lens;
@@ -108,38 +116,56 @@ struct Params {
 #endif
 };
 
-// Shared memory.  The TMA-staged value columns of Q[:, D_r] (4 boxes of 128 heads x 128 B) are
-// moved into TMEM by the softmax warps before the region is reused; the rope columns of Q stay
-// in shared memory (A operand of the two rope k-steps), as does P (A operand of P.V).
+// Shared memory.  The TMA-staged value columns of Q[:, D_r] (4 boxes of 128 heads x 128 B, 64 KiB)
+// land in the score-exchange and P buffers, which are idle until Q has moved into TMEM; the rope
+// columns of Q stay in shared memory (A operand of the two rope k-steps), as does P (A operand of
+// P.V).  The total is exactly the 227 KiB a CTA may use (with 1 KiB of alignment slack).
 struct Layout {
   static constexpr int stages = 0;
-  static constexpr int xbuf = stages + kStages * kTileBytes;  // [kXBufs][16][128] x 16 B
-  static constexpr int pbuf = xbuf + kXBufs * 16 * kHeads * 16;  // P[2]: 128 heads x 128 B, SW128
+  static constexpr int xbuf = stages + kStages * kTileBytes;   // [2][8 chunks][128 heads] x 16 B
+  static constexpr int pbuf = xbuf + 2 * 8 * kHeads * 16;      // P[2]: 128 heads x 128 B, SW128
   static constexpr int qrope = pbuf + 2 * kHeads * 128;  // Q rope half: 128 x 64 B, 64-byte swizzle
   static constexpr int rows = qrope + kHeads * kRopeHalf * 2;
-  static constexpr int qstage = kQInRing ? stages + (kStages - 2) * kTileBytes : xbuf;
-  static constexpr int masks = rows + kMaxRows * 4;       // one 32-bit validity word per 32 slots
-  static constexpr int rowmax = masks + kMaxRows / 8;     // [2][128] tile row maxima
-  static constexpr int ctl = rowmax + 2 * kHeads * 4;
+  static constexpr int qstage = xbuf;                    // 64 KiB: xbuf + pbuf
+  static constexpr int mxr = rows + kMaxRows * 4;       // [2][128] the peer's row maxima; at the
+                                                         // end its partial row sums
+  static constexpr int mref = mxr + 2 * kHeads * 4;     // [128] reference maxima between teams
+  static constexpr int ctl = mref + kHeads * 4;
   static constexpr int total = ctl + 512;
+  // epilogue, in the idle ring: staged O rows [0, 128 KiB), then the lse of every head and the
+  // other split's lse of the heads this CTA finalises (cluster merge), then 1/l of every head
+  static constexpr int lsebuf = stages + kHeads * 1024;
+  static constexpr int invbuf = lsebuf + 192 * 4;
 };
+static_assert(2 * 8 * kHeads * 16 + 2 * kHeads * 128 >= 4 * kHeads * 128, "Q staging");
+static_assert(Layout::invbuf + 128 * 4 <= Layout::stages + kStages * kTileBytes, "lse in the ring");
 
 struct Ctl {
   uint64_t qbar, q_tmem;
   uint64_t full[kStages], empty[kStages];
-  uint64_t s_full[2], s_sum[2], s_free[2], p_full[2], pv_done[2], drain;
-  uint64_t xfull[kXBufs];  // the peer has written its partial S into this CTA's buffer
-  uint64_t xfree[kXBufs];  // the peer has consumed this CTA's previous write into its buffer
+  uint64_t s_full[2], s_free[2];
+  uint64_t xfull[2];   // the peer's partial S of our columns has arrived in xbuf[b]
+  uint64_t xfree[2];   // the peer has consumed what we stored into its xbuf[b]
+  uint64_t mx[2];      // the peer's row maxima of tile buffer b have arrived in mxr[b]
+  uint64_t p_full[2];  // our columns of P buffer b are written (and O rescaled): P.V may run once
+  uint64_t p_rem[2];   // ... the peer's columns of P have arrived too
+  uint64_t pfree[2];   // the peer's P.V has read its P buffer b: we may store into it again
+  uint64_t hand[2];    // team b has left the reference maximum of its latest tile in mref
+  uint64_t pv_done[2], drain, fin, mxdone;
+#ifdef DSA_TEST_HOOKS
+  uint64_t never;      // test build: no thread ever arrives here
+#endif
   uint32_t tmem_base;
   int abort;
-  int last;  // this CTA merges the splits
-  int nvalid;
-  int gather_go[2];  // poller's verdict per step (read by all gather threads after bar.sync)
-  uint64_t mrg;      // cluster merge: the other split's rows and lse have arrived
-#ifdef DSA_TEST_HOOKS
-  uint64_t never;    // test build: no thread ever arrives here
-#endif
+  int nvalid;          // rows up to the last valid slot; at the end: this CTA merges the splits
+  int gather_go;       // the gather poller's verdict of step i in bit i & 1
 };
+static_assert(sizeof(Ctl) <= 512, "control block");
+
+// Cluster merge (two row splits): workspace slot of (token t, value half r, split s) holding the
+// normalised rows of the 64 heads the other split finalises ([64][256] fp32) and their lse.
+constexpr int kCmRowFloats = kDvHalf;
+DSA_DEV size_t cm_slot(int t, int r, int s) { return ((size_t)t * 2 + r) * 2 + s; }
 
 DSA_DEV int find_seq(const int* q_start, int B, int t) {
   int lo = 0, hi = B - 1;
@@ -198,6 +224,21 @@ DSA_DEV uint32_t dequant2(uint32_t codes2, float scale) {
   return pack_bf16(f.x * scale, f.y * scale);
 }
 
+// O row of TMEM lane `lane_addr`, columns [col0, col0 + 128), times `alpha`.
+DSA_DEV void rescale_o(uint32_t lane_addr, uint32_t col0, float alpha) {
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t o[32];
+    tmem_ld_x32(lane_addr + col0 + (uint32_t)(cc * 32), o);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+    tmem_st_x16(lane_addr + col0 + (uint32_t)(cc * 32), o);
+    tmem_st_x16(lane_addr + col0 + (uint32_t)(cc * 32 + 16), o + 16);
+  }
+  tmem_st_wait();
+}
+
 template <bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
@@ -208,7 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* st_s = smem + Layout::stages;
   uint4* xbuf = reinterpret_cast<uint4*>(smem + Layout::xbuf);
   int* rows_s = reinterpret_cast<int*>(smem + Layout::rows);
-  uint32_t* masks_s = reinterpret_cast<uint32_t*>(smem + Layout::masks);
+  float* mxr = reinterpret_cast<float*>(smem + Layout::mxr);
+  float* mref = reinterpret_cast<float*>(smem + Layout::mref);
+  float* lsebuf = reinterpret_cast<float*>(smem + Layout::lsebuf);
+  float* invbuf = reinterpret_cast<float*>(smem + Layout::invbuf);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + Layout::ctl);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -228,24 +272,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->full[s], kGatherThreads);
       mbar_init(&ctl->empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 2; ++b) {       // buffer b: tiles i with i % 2 == b, score team b
       mbar_init(&ctl->s_full[b], 1);
-      mbar_init(&ctl->s_sum[b], 128);
-      mbar_init(&ctl->s_free[b], 128);
-      mbar_init(&ctl->p_full[b], 128);
+      mbar_init(&ctl->s_free[b], 128);  // team b
+      mbar_init(&ctl->xfull[b], 1);     // one local expect_tx arrival + the peer's stored bytes
+      mbar_init(&ctl->xfree[b], 128);   // the peer's team b
+      mbar_init(&ctl->mx[b], 1);
+      mbar_init(&ctl->p_full[b], 128);  // team b
+      mbar_init(&ctl->p_rem[b], 1);
+      mbar_init(&ctl->pfree[b], 128);   // the peer's team b
+      mbar_init(&ctl->hand[b], 128);    // team b
       mbar_init(&ctl->pv_done[b], 1);
     }
     mbar_init(&ctl->drain, 1);
-    for (int x = 0; x < kXBufs; ++x) {
-      mbar_init(&ctl->xfull[x], 1);  // one local expect_tx arrival + the peer's stored bytes
-      mbar_init(&ctl->xfree[x], 128);
-    }
-    mbar_init(&ctl->mrg, 1);
+    mbar_init(&ctl->fin, 1);
+    mbar_init(&ctl->mxdone, 256);       // both teams of the peer have read their last maxima
+    // The peer's P columns of tiles 0 and 1; the MMA thread, which observes each phase complete,
+    // arms the next phase of a buffer when it consumes one.
+    mbar_arrive_expect_tx(&ctl->p_rem[0], kPRemBytes);
+    mbar_arrive_expect_tx(&ctl->p_rem[1], kPRemBytes);
 #ifdef DSA_TEST_HOOKS
     mbar_init(&ctl->never, 1);
 #endif
     ctl->abort = 0;
     ctl->nvalid = 0;
+    ctl->gather_go = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -253,18 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   __syncthreads();  // barriers initialised
-  // merge buffers: 64 rows of the other split (64 KiB) and its 64 lse values (256 B)
-  if (p.cluster_merge && tid == 0) mbar_arrive_expect_tx(&ctl->mrg, 64 * 1024 + 64 * 4);
   cluster_sync();   // ... in every CTA of the cluster before any remote arrive
   // The launch may overlap the end of the preceding kernel in the stream (programmatic dependent
   // launch): everything above touches only this CTA's resources; no global memory is read
   // before the preceding kernel has completed and its writes are visible.
   griddep_wait();
-  const int b = find_seq(p.q_start, p.B, t);
-  const int L = min(p.seq_lens[b], p.max_pages * 64);  // positions the page table covers
+  const int b_seq = find_seq(p.q_start, p.B, t);
+  const int L = min(p.seq_lens[b_seq], p.max_pages * 64);  // positions the page table covers
   if (warp == kMmaWarp && lane == 0 && nslot > 0) {
-    // value columns of Q[:, D_r] -> shared memory (moved into TMEM by the softmax warps);
-    // issued before the row translation below so the load overlaps it
+    // value columns of Q[:, D_r] -> shared memory (moved into TMEM by warps 12-15); issued before
+    // the row translation below so the load overlaps it
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_qr);
     mbar_arrive_expect_tx(&ctl->qbar, 4 * kHeads * 128 + kHeads * kRopeHalf * 2);
@@ -273,8 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   (4 * half + bx) * 64, t * p.H);
     tma_load_2d(smem + Layout::qrope, &tm_qr, &ctl->qbar, kDv + kRopeHalf * half, t * p.H);
   }
-  // logical position -> physical row of every slot of this split (-1: empty or invalid), and a
-  // validity bit per slot (the softmax masks whole tiles from two words, with no per-slot loads)
+  // logical position -> physical row of every slot of this split (-1: empty or invalid)
   // (all index loads of a thread first, then all page-table loads: two round trips)
   int last_valid = -1;
   {
@@ -287,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u)
-      pg[u] = (j[u] >= 0 && j[u] < L) ? p.page_table[(size_t)b * p.max_pages + (j[u] >> 6)] : -1;
+      pg[u] = (j[u] >= 0 && j[u] < L) ? p.page_table[(size_t)b_seq * p.max_pages + (j[u] >> 6)] : -1;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int i = u * kThreads + tid;
@@ -304,8 +352,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows_s[i] = row;
         if (row >= 0) last_valid = i;
       }
-      const uint32_t m = __ballot_sync(0xffffffffu, row >= 0);
-      if (lane == 0) masks_s[i >> 5] = m;
     }
   }
   // tiles needed: up to the last valid slot (the same in both CTAs of the pair)
@@ -318,31 +364,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
 
-  // per-head state (softmax warps): reference maximum, the sum of the bf16 weights P.V uses
-  // (normalisation), and the fp32 sum of the unrounded weights (log-sum-exp)
-  float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
-
   if (warp < 4 || (warp >= 9 && warp < 12)) {
-    // ---------------- gather: 16-byte cp.async of this CTA's 640 bytes of each selected row
+    // ---------------- gather: 16-byte cp.async of this CTA's 576 bytes of each selected row
     // into the ring, 128-byte swizzled [box][row][128 B] so the tile is a valid tcgen05 operand
     const int g = warp < 4 ? tid : tid - 9 * 32 + 128;  // 0 .. kGatherThreads - 1
     const uint8_t* kv = reinterpret_cast<const uint8_t*>(p.kv);
     // One thread polls each barrier; the other gather warps sleep on a hardware barrier and
-    // then read the poller's verdict (a slot that is not rewritten before every gather thread
-    // has passed the next bar.sync, so all of them leave the loop at the same step).
+    // then read the poller's verdict (bit i & 1 of gather_go, which is not rewritten before
+    // every gather thread has passed the next bar.sync, so all of them leave at the same step).
     for (int i = 0; i < ntile; ++i) {
       const int s = i % kStages;
-      if (i >= kStages || (kQInRing && i >= kStages - 2)) {
-        // a reused stage waits for the P.V that read it; a stage holding Q waits for TMEM
-        if (g == 0)
-          ctl->gather_go[i & 1] =
-              (i >= kStages
-                   ? mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status)
-                   : mbar_wait(&ctl->q_tmem, 0, abort, p.status))
-                  ? 1
-                  : 0;
+      if (i >= kStages) {
+        // a reused stage waits for the P.V that read it
+        if (g == 0) {
+          const int v = mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status) ? 1 : 0;
+          volatile int* go = &ctl->gather_go;
+          *go = (*go & ~(1 << (i & 1))) | (v << (i & 1));
+        }
         named_barrier(1, kGatherThreads);
-        if (*reinterpret_cast<volatile int*>(&ctl->gather_go[i & 1]) == 0) break;
+        if (((*reinterpret_cast<volatile int*>(&ctl->gather_go) >> (i & 1)) & 1) == 0) break;
       }
       const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
       if constexpr (KV8) {
@@ -401,169 +441,140 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == kMmaWarp && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc_qk = idesc_bf16(128, kNT);
-    constexpr uint32_t idesc_pv = idesc_bf16(128, kDvHalf, /*b_mn_major=*/true);
-    // Descriptors are built once; a k-step only moves the start address (the 14-bit address
-    // field cannot carry: every operand lies below 256 KiB).
-    const uint64_t st_desc = sdesc_sw128(smem_u32(st_s), 16, 1024);
-    const uint64_t v_desc = sdesc_sw128(smem_u32(st_s), kBoxBytes, 1024);
-    const uint64_t qr_desc = sdesc_sw64(smem_u32(smem + Layout::qrope), 512);
-    const uint64_t rope_desc = sdesc_sw64(smem_u32(st_s) + 4u * kBoxBytes, 512);
-    const uint64_t p_desc = sdesc_sw128(smem_u32(smem + Layout::pbuf), 16, 1024);
-    bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc_qk = idesc_bf16(128, kNT);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, kDvHalf, /*b_mn_major=*/true);
+      // Descriptors are built once; a k-step only moves the start address (the 14-bit address
+      // field cannot carry: every operand lies below 256 KiB).
+      const uint64_t st_desc = sdesc_sw128(smem_u32(st_s), 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(smem_u32(st_s), kBoxBytes, 1024);
+      const uint64_t qr_desc = sdesc_sw64(smem_u32(smem + Layout::qrope), 512);
+      const uint64_t rope_desc = sdesc_sw64(smem_u32(st_s) + 4u * kBoxBytes, 512);
+      const uint64_t p_desc = sdesc_sw128(smem_u32(smem + Layout::pbuf), 16, 1024);
+      bool ok = nslot == 0 || mbar_wait(&ctl->qbar, 0, abort, p.status);  // no TMA left in flight
 #ifdef DSA_TEST_HOOKS
-    if (p.stall == 2 && blockIdx.x == 0) ok = ok && mbar_wait(&ctl->never, 0, abort, p.status);
+      if (p.stall == 2 && blockIdx.x == 0) ok = ok && mbar_wait(&ctl->never, 0, abort, p.status);
 #endif
-    ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
-    // Issue whichever is ready: P.V of the oldest tile whose weights are written (needs P; it
-    // releases a ring stage) is tested first, then Q.K^T of the next tile (needs its rows and a
-    // free S buffer).
-    int nqk = 0, npv = 0;
-    uint64_t t_idle = 0;
-    while (ok && npv < ntile) {
-      bool progressed = false;
-      if (npv < nqk && mbar_test(&ctl->p_full[npv & 1], (uint32_t)(npv >> 1) & 1u)) {
-        tc_fence_after();
-        const int s = npv % kStages;
-        const uint64_t vb = v_desc + (uint64_t)((s * kTileBytes) >> 4);
+      ok = ok && (ntile == 0 || mbar_wait(&ctl->q_tmem, 0, abort, p.status));
+      // Issue whichever is ready: P.V of the oldest tile whose weights are written (needs P; it
+      // releases a ring stage) is tested first, then Q.K^T of the next tile (needs its rows and a
+      // free S buffer).
+      int nqk = 0, npv = 0;
+      uint64_t t_idle = 0;
+      while (ok && npv < ntile) {
+        bool progressed = false;
+        if (npv < nqk && mbar_test(&ctl->p_full[npv & 1], (uint32_t)(npv >> 1) & 1u) &&
+            mbar_test_cluster(&ctl->p_rem[npv & 1], (uint32_t)(npv >> 1) & 1u)) {
+          // our P columns were stored by threads of this CTA, the peer's by st.async: both are
+          // read by the tensor core (async proxy)
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const int s = npv % kStages;
+          const uint64_t vb = v_desc + (uint64_t)((s * kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kNT / 16; ++kk) {
-          // A = P (K-major, keys [16kk, 16kk+16)); B = V rows [16kk, 16kk+16) x this half's 256
-          // value columns, MN-major: 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024
-          // bytes apart (sbo)
-          mma_f16_ss(tmem + kColO, p_desc + (uint64_t)(((npv & 1) * kHeads * 128 + kk * 32) >> 4),
-                     vb + (uint64_t)(kk * 2048 >> 4),
-                     idesc_pv, (npv > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kNT / 16; ++kk) {
+            // A = P (K-major, keys [16kk, 16kk+16)); B = V rows [16kk, 16kk+16) x this half's 256
+            // value columns, MN-major: 64-column blocks kBoxBytes apart (lbo), 8-row groups 1024
+            // bytes apart (sbo)
+            mma_f16_ss(tmem + kColO, p_desc + (uint64_t)(((npv & 1) * kHeads * 128 + kk * 32) >> 4),
+                       vb + (uint64_t)(kk * 2048 >> 4),
+                       idesc_pv, (npv > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&ctl->pv_done[npv & 1]);
+          mma_commit(&ctl->empty[s]);
+          // the phase of p_rem for tile npv is complete: arm the one of tile npv + 2
+          if (npv + 2 < ntile) mbar_arrive_expect_tx(&ctl->p_rem[npv & 1], kPRemBytes);
+          ++npv;
+          progressed = true;
         }
-        mma_commit(&ctl->pv_done[npv & 1]);
-        mma_commit(&ctl->empty[s]);
-        ++npv;
-        progressed = true;
-      }
-      if (nqk < ntile && mbar_test(&ctl->full[nqk % kStages], (uint32_t)(nqk / kStages) & 1u) &&
-          (nqk < 2 || mbar_test(&ctl->s_free[nqk & 1], (uint32_t)((nqk >> 1) - 1) & 1u))) {
-        // the tile was written by cp.async (generic proxy); tcgen05.mma reads it (async proxy)
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t sbase = (uint32_t)((nqk % kStages) * kTileBytes);
-        const uint32_t d_s = tmem + kColS + (uint32_t)((nqk & 1) * kNT);
+        if (nqk < ntile && mbar_test(&ctl->full[nqk % kStages], (uint32_t)(nqk / kStages) & 1u) &&
+            (nqk < 2 || mbar_test(&ctl->s_free[nqk & 1], (uint32_t)((nqk >> 1) - 1) & 1u))) {
+          // the tile was written by cp.async (generic proxy); tcgen05.mma reads it (async proxy)
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t sbase = (uint32_t)((nqk % kStages) * kTileBytes);
+          const uint32_t d_s = tmem + kColS + (uint32_t)((nqk & 1) * kNT);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {  // the value boxes, A = Q from TMEM
-          const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-          mma_f16_ts(d_s, tmem + kColQ + (uint32_t)kk * 8u, st_desc + ((sbase + off) >> 4), idesc_qk,
-                     kk > 0 ? 1u : 0u);
-        }
+          for (int kk = 0; kk < 16; ++kk) {  // the value boxes, A = Q from TMEM
+            const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+            mma_f16_ts(d_s, tmem + kColQ + (uint32_t)kk * 8u, st_desc + ((sbase + off) >> 4), idesc_qk,
+                       kk > 0 ? 1u : 0u);
+          }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)  // this CTA's rope half, A = Q from shared memory
-          mma_f16_ss(d_s, qr_desc + (uint64_t)(kk * 2), rope_desc + (uint64_t)((sbase >> 4) + kk * 2),
-                     idesc_qk, 1u);
-        mma_commit(&ctl->s_full[nqk & 1]);
-        ++nqk;
-        progressed = true;
-      }
-      if (progressed) {
-        t_idle = 0;
-      } else {
-        const uint64_t now = globaltimer();
-        if (t_idle == 0) t_idle = now;
-        if (*abort) break;
-        if (now - t_idle > kWaitLimitNs) {
-          *abort = 1;
-          report(p.status, kStatusTimeout);
-          break;
+          for (int kk = 0; kk < 2; ++kk)  // this CTA's rope half, A = Q from shared memory
+            mma_f16_ss(d_s, qr_desc + (uint64_t)(kk * 2), rope_desc + (uint64_t)((sbase >> 4) + kk * 2),
+                       idesc_qk, 1u);
+          mma_commit(&ctl->s_full[nqk & 1]);
+          ++nqk;
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          const uint64_t now = globaltimer();
+          if (t_idle == 0) t_idle = now;
+          if (*abort) break;
+          if (now - t_idle > kWaitLimitNs) {
+            *abort = 1;
+            report(p.status, kStatusTimeout);
+            break;
+          }
         }
       }
+      mma_commit(&ctl->drain);
+      mbar_wait(&ctl->drain, 0, abort, p.status);
     }
-    mma_commit(&ctl->drain);
-    mbar_wait(&ctl->drain, 0, abort, p.status);
-  } else if (warp >= kXchgWarp0 && warp < kXchgWarp0 + 4) {
-    // ---------------- score exchange: one thread per head row (TMEM lane quadrant warp % 4),
-    // running ahead of the softmax.  The partial row goes into the peer's buffer (asynchronous
-    // stores that count their bytes on the peer's xfull), the peer's partial is added in the same
-    // order in both CTAs (S_0 + S_1), and the masked, scaled row z goes back into the tile's S
-    // columns with its maximum in shared memory.
-    // Buffer layout [x][chunk c of 4 columns][head] x 16 B: a warp's stores and loads are
-    // contiguous.
-    const int h = (warp - kXchgWarp0) * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp - kXchgWarp0) * 32) << 16);
-    const uint32_t peer_xbuf = map_cluster(xbuf, peer);
-    const uint32_t peer_xfull = map_cluster(&ctl->xfull[0], peer);
-    const uint32_t peer_xfree = map_cluster(&ctl->xfree[0], peer);
-    if (ntile > 0) {
-#pragma unroll
-      for (int x = 0; x < kXBufs; ++x) mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);
-    }
-    for (int i = 0; i < ntile; ++i) {
-      const int x = i % kXBufs;
-      const uint32_t xph = (uint32_t)(i / kXBufs) & 1u;
-      bool ok = mbar_wait(&ctl->s_full[i & 1], (uint32_t)(i >> 1) & 1u, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc_fence_after();
-      uint32_t sr[64];
-      const uint32_t s_col = kColS + (uint32_t)((i & 1) * kNT);
-      tmem_ld_x32(lane_addr + s_col, sr);
-      tmem_ld_x32(lane_addr + s_col + 32, sr + 32);
-      tmem_ld_wait();
-      if (h == 0) mbar_arrive_expect_tx(&ctl->xfull[x], 16u * kHeads * 16u);
-      ok = mbar_wait<true>(&ctl->xfree[x], xph, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_async_v4(peer_xbuf + (uint32_t)(((x * 16 + c) * kHeads + h) * 16),
-                    make_uint4(sr[4 * c], sr[4 * c + 1], sr[4 * c + 2], sr[4 * c + 3]),
-                    peer_xfull + 8u * (uint32_t)x);
-      ok = mbar_wait<true>(&ctl->xfull[x], xph, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      // z = S * scale * log2(e) for valid slots, -inf for empty ones; and the row maximum
-      float mk[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
-      const uint32_t vm0 = masks_s[2 * i], vm1 = masks_s[2 * i + 1];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 o = xbuf[(x * 16 + c) * kHeads + h];
-        const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int col = 4 * c + k;
-          const float a = __uint_as_float(sr[col]), b2 = __uint_as_float(ov[k]);
-          const float sv = half == 0 ? a + b2 : b2 + a;
-          const bool valid = ((col < 32 ? vm0 : vm1) >> (col & 31)) & 1u;
-          const float z = valid ? sv * p.scale_log2 : -INFINITY;
-          sr[col] = __float_as_uint(z);
-          mk[k] = fmaxf(mk[k], z);
-        }
-      }
-      const float mt = fmaxf(fmaxf(mk[0], mk[1]), fmaxf(mk[2], mk[3]));
-      mbar_arrive_remote_relaxed(peer_xfree + 8u * (uint32_t)x);  // our buffer x may be rewritten
-      reinterpret_cast<float*>(smem + Layout::rowmax)[(i & 1) * kHeads + h] = mt;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st_x16(lane_addr + s_col + (uint32_t)(16 * c), sr + 16 * c);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&ctl->s_sum[i & 1]);
-    }
-  } else if (warp >= kSoftmaxWarp0) {
-    // ---------------- softmax: one thread per head row (TMEM lane)
-    const int qd = warp - kSoftmaxWarp0, h = qd * 32 + lane;
+    __syncwarp();  // the warp is converged again before the aligned cluster barrier
+  } else {
+    // ---------------- score warps 4-7 (team 0: even tiles) and 12-15 (team 1: odd tiles), one
+    // thread per head row h = TMEM lane (quadrant warp % 4).  The pair splits each 64-row tile by
+    // columns: this CTA finalises the softmax of columns [32 half, 32 half + 32) for every head,
+    // so the exponentials spread over all four lane quadrants (each served by its own SM
+    // sub-partition), and the two teams take alternate tiles, so that one tile's exchanges with
+    // the peer overlap the next tile's.  For a tile, a thread:
+    //   - sends our partial of the peer's columns of its row to the peer;
+    //   - adds the peer's partial of our columns (always S_0 + S_1), masks and scales them;
+    //   - exchanges the row maximum of our columns with the peer (both CTAs then hold the same
+    //     tile maximum and take the same rescale decisions);
+    //   - takes the reference maximum left by the other team's tile, moves it lazily (only
+    //     when exceeded by more than 2^8, then rescaling O) and leaves it to the other team;
+    //   - writes our columns of P (bf16) into our P buffer and the peer's.
+    const int qd = warp & 3;                 // TMEM lane quadrant
+    const int team = warp >= 12 ? 1 : 0;     // tiles i with i % 2 == team; also P / xbuf buffer
+    const int h = qd * 32 + lane;            // head = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(qd * 32) << 16);
-    if (ntile > 0) {
+    const uint32_t col_fin = (uint32_t)(kFinCols * half);        // our columns of a tile
+    const uint32_t col_snd = (uint32_t)(kFinCols * (half ^ 1));  // the peer's
+    const uint32_t peer_xbuf = map_cluster(xbuf, peer);
+    const uint32_t peer_pbuf = map_cluster(smem + Layout::pbuf, peer);
+    const uint32_t peer_mxr = map_cluster(mxr, peer);
+    const uint32_t peer_xfull = map_cluster(&ctl->xfull[team], peer);
+    const uint32_t peer_xfree = map_cluster(&ctl->xfree[team], peer);
+    const uint32_t peer_mx = map_cluster(&ctl->mx[team], peer);
+    const uint32_t peer_prem = map_cluster(&ctl->p_rem[team], peer);
+    const uint32_t peer_pfree = map_cluster(&ctl->pfree[team], peer);
+    const uint32_t peer_finbar = map_cluster(&ctl->fin, peer);
+    const uint32_t peer_mxdone = map_cluster(&ctl->mxdone, peer);
+    const int b = team;
+    if (team == 1 && ntile > 0) {
       // Q[t][h][value columns of D_r] -> TMEM columns kColQ.. (two bf16 per 32-bit column) from
       // the TMA-staged boxes (128-byte swizzled); heads >= H are 0.
       const bool ok = mbar_wait(&ctl->qbar, 0, abort, p.status);
       (void)ok;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t r[32];
-        const uint8_t* box = smem + Layout::qstage + c * (kHeads * 128) + h * 128;
+        const uint8_t* box = smem + Layout::qstage + cc * (kHeads * 128) + h * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = h < p.H ? *reinterpret_cast<const uint4*>(box + ((v ^ (h & 7)) << 4))
                                   : make_uint4(0u, 0u, 0u, 0u);
           r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
         }
-        tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32), r);
-        tmem_st_x16(lane_addr + kColQ + (uint32_t)(c * 32 + 16), r + 16);
+        tmem_st_x16(lane_addr + kColQ + (uint32_t)(cc * 32), r);
+        tmem_st_x16(lane_addr + kColQ + (uint32_t)(cc * 32 + 16), r + 16);
       }
       if (h >= p.H) {  // padded heads: zero rope row (the staged rows belong to the next token)
 #pragma unroll
@@ -576,93 +587,201 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&ctl->q_tmem);
     }
-    for (int i = 0; i < ntile; ++i) {
-      // z of this tile (S_0 + S_1, masked and scaled) and its row maximum, from the exchange warps
-      bool ok = mbar_wait(&ctl->s_sum[i & 1], (uint32_t)(i >> 1) & 1u, abort, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
+    if (ntile > b) {
+      // Our exchange and P buffers hold the staged Q until it is in TMEM; then the peer may
+      // store into our exchange buffer of this team (its initial credit).
+      mbar_wait(&ctl->q_tmem, 0, abort, p.status);
+      mbar_arrive_remote_relaxed(peer_xfree);
+    }
+    // this team's sums over our columns of the bf16 weights P.V uses (normalisation) and of the
+    // unrounded weights (log-sum-exp), relative to the reference m_ref
+    float m_ref = -INFINITY, l_sum = 0.f, l_exact = 0.f;
+    for (int i = team; i < ntile; i += 2) {
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[b], ph, abort, p.status));
+      if (!ok) break;
+      uint32_t sr[32], sp[32];
       tc_fence_after();
-      uint32_t sr[64];
-      const uint32_t s_col = kColS + (uint32_t)((i & 1) * kNT);
-      tmem_ld_x32(lane_addr + s_col, sr);
-      tmem_ld_x32(lane_addr + s_col + 32, sr + 32);
-      const float mt = reinterpret_cast<const float*>(smem + Layout::rowmax)[(i & 1) * kHeads + h];
+      tmem_ld_x32(lane_addr + kColS + (uint32_t)(b * kNT) + col_fin, sr);
+      tmem_ld_x32(lane_addr + kColS + (uint32_t)(b * kNT) + col_snd, sp);
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&ctl->s_free[i & 1]);
-      // lazy rescale: move the reference maximum only when it is exceeded by more than 2^8
-      const bool need = mt > m_ref + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need && i >= 1 && l_sum > 0.f)) {
-        // O is rewritten: every P.V so far must have landed
-        ok = mbar_wait(&ctl->pv_done[(i - 1) & 1], (uint32_t)((i - 1) >> 1) & 1u, abort, p.status);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      mbar_arrive(&ctl->s_free[b]);
+      if (h == 0) {  // (this thread observed the previous phases of both complete)
+        mbar_arrive_expect_tx(&ctl->xfull[b], kXBytes);
+        mbar_arrive_expect_tx(&ctl->mx[b], kMxBytes);
+      }
+      // our partial of the peer's columns -> the peer's xbuf[b], chunk k of 4 columns at
+      // [b][k][head] (a warp stores 512 contiguous bytes per chunk)
+      ok = __all_sync(0xffffffffu, mbar_wait<true>(&ctl->xfree[b], ph, abort, p.status));
+      if (!ok) break;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        st_async_v4(peer_xbuf + (uint32_t)(((b * 8 + k) * kHeads + h) * 16),
+                    make_uint4(sp[4 * k], sp[4 * k + 1], sp[4 * k + 2], sp[4 * k + 3]), peer_xfull);
+      // validity of our 32 slots of the tile (one row-table entry per lane)
+      const int slot = i * kNT + (int)col_fin + lane;
+      const uint32_t vm = __ballot_sync(0xffffffffu, slot < nslot && rows_s[slot] >= 0);
+      ok = __all_sync(0xffffffffu, mbar_wait<true>(&ctl->xfull[b], ph, abort, p.status));
+      if (!ok) break;
+      // z = (S_0 + S_1) * scale * log2(e) for valid slots, -inf for empty ones
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 o = xbuf[(b * 8 + k) * kHeads + h];
+        const uint32_t ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int col = 4 * k + e;
+          const float a = __uint_as_float(sr[col]), b2 = __uint_as_float(ov[e]);
+          const float sv = half == 0 ? a + b2 : b2 + a;
+          const bool valid = (vm >> col) & 1u;
+          const float z = valid ? sv * p.scale_log2 : -INFINITY;
+          sr[col] = __float_as_uint(z);
+          m4[e] = fmaxf(m4[e], z);
+        }
+      }
+      const float mk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      mbar_arrive_remote_relaxed(peer_xfree);  // our xbuf[b] may be refilled
+      // the tile's row maximum: ours to the peer, the peer's back
+      st_async_b32(peer_mxr + (uint32_t)((b * kHeads + h) * 4), __float_as_uint(mk), peer_mx);
+      ok = __all_sync(0xffffffffu, mbar_wait<true>(&ctl->mx[b], ph, abort, p.status));
+      if (!ok) break;
+      const float mt = fmaxf(mk, mxr[b * kHeads + h]);
+      // the reference maximum after the previous tile (the other team's)
+      float m_cur = -INFINITY;
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->hand[b ^ 1], (uint32_t)((i - 1) >> 1) & 1u,
+                                               abort, p.status));
+        if (!ok) break;
+        m_cur = mref[h];
+      }
+      // lazy rescale: move the reference only when it is exceeded by more than 2^8 (the same
+      // decision in both CTAs: both see the same maximum)
+      const bool need = mt > m_cur + kRescaleLog2;
+      const float m_new = need ? mt : m_cur;
+      mref[h] = m_new;
+      mbar_arrive(&ctl->hand[b]);  // the other team's next tile may take it
+      const bool resc = need && m_cur != -INFINITY;  // O holds weights of an older reference
+      if (__any_sync(0xffffffffu, resc)) {  // implies i >= 1
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[b ^ 1], (uint32_t)((i - 1) >> 1) & 1u,
+                                               abort, p.status));
+        if (!ok) break;
         tc_fence_after();
-        const float alpha = (need && l_sum > 0.f) ? exp2f(m_ref - mt) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < kDvHalf / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_x32(lane_addr + kColO + (uint32_t)(c * 32), o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          tmem_st_x16(lane_addr + kColO + (uint32_t)(c * 32), o);
-          tmem_st_x16(lane_addr + kColO + (uint32_t)(c * 32 + 16), o + 16);
-        }
-        tmem_st_wait();
-        if (need) {
-          l_sum *= alpha;
-          l_exact *= alpha;
-        }
+        const float alpha = resc ? exp2f(m_cur - m_new) : 1.f;
+        rescale_o(lane_addr, kColO, alpha);
+        rescale_o(lane_addr, kColO + 128u, alpha);
       }
-      if (need) m_ref = mt;
-      uint32_t pk[32];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f}, le[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * c]) - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * c + 1]) - m_ref);
-        pk[c] = pack_bf16(p0, p1);
-        const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&pk[c]);
-        ls[c & 3] += __bfloat162float(r.x) + __bfloat162float(r.y);
-        le[c & 3] += p0 + p1;
+      if (m_ref != m_new) {  // this team's sums follow the reference
+        if (m_ref != -INFINITY) {
+          const float f = exp2f(m_ref - m_new);
+          l_sum *= f;
+          l_exact *= f;
+        }
+        m_ref = m_new;
       }
-      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      l_exact += (le[0] + le[1]) + (le[2] + le[3]);
-      // P row h -> shared memory buffer i & 1, 128-byte swizzled K-major (the A operand of P.V),
-      // once the P.V that read it two tiles ago has landed
+      uint32_t pk[16];
+      float ls[2] = {0.f, 0.f}, le[2] = {0.f, 0.f};  // independent chains
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const float p0 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * cc]) - m_ref);
+        const float p1 = m_ref == -INFINITY ? 0.f : fast_exp2(__uint_as_float(sr[2 * cc + 1]) - m_ref);
+        pk[cc] = pack_bf16(p0, p1);
+        const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&pk[cc]);
+        ls[cc & 1] += __bfloat162float(r.x) + __bfloat162float(r.y);
+        le[cc & 1] += p0 + p1;
+      }
+      l_sum += ls[0] + ls[1];
+      l_exact += le[0] + le[1];
       if (i >= 2) {
-        ok = mbar_wait(&ctl->pv_done[i & 1], (uint32_t)((i - 2) >> 1) & 1u, abort, p.status);
+        // P buffer b was read by the P.V two tiles back: ours (the peer may write its columns
+        // into it again), and the peer's (it says so)
+        ok = mbar_wait(&ctl->pv_done[b], (uint32_t)((i - 2) >> 1) & 1u, abort, p.status);
+        mbar_arrive_remote_relaxed(peer_pfree);
+        ok = mbar_wait<true>(&ctl->pfree[b], (uint32_t)((i >> 1) - 1) & 1u, abort, p.status) && ok;
         if (!__all_sync(0xffffffffu, ok)) break;
       }
-      uint8_t* prow = smem + Layout::pbuf + (i & 1) * (kHeads * 128) + h * 128;
+      // P row h, our columns = 16-byte chunks 4 half .. 4 half + 3 of the 128-byte row (the A
+      // operand of P.V, 128-byte swizzle), into our buffer and the peer's
+      const uint32_t row_off = (uint32_t)(b * (kHeads * 128) + h * 128);
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        *reinterpret_cast<uint4*>(prow + ((v ^ (h & 7)) << 4)) =
-            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      for (int v = 0; v < 4; ++v) {
+        const uint32_t off = row_off + (uint32_t)((((4 * half + v) ^ (h & 7))) << 4);
+        const uint4 val = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        *reinterpret_cast<uint4*>(smem + Layout::pbuf + off) = val;
+        st_async_v4(peer_pbuf + off, val, peer_prem);
+      }
       fence_proxy_async_smem();
-      mbar_arrive(&ctl->p_full[i & 1]);
+      tc_fence_before();
+      mbar_arrive(&ctl->p_full[b]);
     }
+    // we have read our last maxima: the peer may now store its row sums over them
+    mbar_arrive_remote_relaxed(peer_mxdone);
+    // Row sums of each head over all columns: both teams' (at the final reference) and the
+    // peer's, added in the same order in both CTAs (team 0 first, CTA 0 first), so both
+    // normalise with the same 1/l and report the same lse.
+    named_barrier(3, 256);  // both teams are done: the final reference is in mref
+    const float m_fin = ntile > 0 ? mref[h] : -INFINITY;
+    if (m_ref != m_fin && m_ref != -INFINITY) {
+      const float f = exp2f(m_ref - m_fin);
+      l_sum *= f;
+      l_exact *= f;
+    }
+    float2* team_sums = reinterpret_cast<float2*>(xbuf);  // idle: every partial was consumed
+    if (team == 1) team_sums[h] = make_float2(l_sum, l_exact);
+    named_barrier(3, 256);
+    float inv = 0.f, lse2 = -INFINITY;
+    if (team == 0) {
+      const float2 t1 = team_sums[h];
+      l_sum = l_sum + t1.x;
+      l_exact = l_exact + t1.y;
+      if (h == 0) mbar_arrive_expect_tx(&ctl->fin, kFinBytes);
+      // the peer has read its last maxima from the buffer our sums go to
+      bool ok = ntile == 0 || mbar_wait<true>(&ctl->mxdone, 0, abort, p.status);
+      if (ok) {
+        st_async_b32(peer_mxr + (uint32_t)(h * 4), __float_as_uint(l_sum), peer_finbar);
+        st_async_b32(peer_mxr + (uint32_t)((kHeads + h) * 4), __float_as_uint(l_exact), peer_finbar);
+      }
+      ok = ok && mbar_wait<true>(&ctl->fin, 0, abort, p.status);
+      if (ok) {
+        const float ls_p = mxr[h], le_p = mxr[kHeads + h];
+        const float Ls = half == 0 ? l_sum + ls_p : ls_p + l_sum;
+        const float Le = half == 0 ? l_exact + le_p : le_p + l_exact;
+        inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        lse2 = Le > 0.f ? m_fin + log2f(Le) : -INFINITY;
+      }
+    }
+    // the last P.V has landed in O (and every gathered tile has been consumed: the ring is idle)
     if (ntile > 0) {
       const bool ok =
           mbar_wait(&ctl->pv_done[(ntile - 1) & 1], (uint32_t)((ntile - 1) >> 1) & 1u, abort, p.status);
       (void)__all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
-    // ---------------- epilogue: the normalised O row goes into the (now idle) ring, 16-byte
-    // chunk c of row h at chunk c ^ (h & 31) so that a warp's stores spread over the banks; all
-    // threads then copy the tile out with coalesced stores after the barrier below
-    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    const float lse2 = l_exact > 0.f ? m_ref + log2f(l_exact) : -INFINITY;
+    if (team == 0) {
+      invbuf[h] = inv;
+      lsebuf[h] = lse2;
+    }
+    named_barrier(3, 256);
+    if (team == 1) {
+      inv = invbuf[h];
+      lse2 = lsebuf[h];
+    }
+    const int c = team;  // value columns [128c, 128c + 128) of the head
+    // ---------------- epilogue: the normalised O row (this thread: its 128 value columns) goes
+    // into the (now idle) ring, 16-byte chunk k of row h at chunk k ^ (h & 31) so that a warp's
+    // stores spread over the banks; all threads then copy the tile out with coalesced stores
 #pragma unroll 1
-    for (int c = 0; c < kDvHalf / 32; ++c) {
+    for (int cc = 0; cc < 4; ++cc) {
       uint32_t o[32];
       if (ntile > 0) {
-        tmem_ld_x32(lane_addr + kColO + (uint32_t)(c * 32), o);
+        tmem_ld_x32(lane_addr + kColO + (uint32_t)(128 * c + 32 * cc), o);
         tmem_ld_wait();
       } else {
 #pragma unroll
         for (int k = 0; k < 32; ++k) o[k] = 0u;
       }
-      if (p.splits == 1) {  // bf16 rows of 512 B: chunks 4c .. 4c+3
+      if (p.splits == 1) {  // bf16 rows of 512 B: chunks 16c + 4cc .. +3
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint4 w;
@@ -670,24 +789,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
           w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
           w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-          *reinterpret_cast<uint4*>(st_s + h * 512 + (((4 * c + v) ^ (h & 31)) << 4)) = w;
+          *reinterpret_cast<uint4*>(st_s + h * 512 + (((16 * c + 4 * cc + v) ^ (h & 31)) << 4)) = w;
         }
-      } else {  // fp32 rows of 1 KiB: chunks 8c .. 8c+7
+      } else if (p.cluster_merge && (h >> 6) != split) {
+        // a head the other split finalises: its row goes to our workspace slot for it (L2), while
+        // the cluster's CTAs are still finishing (the 20-byte-per-clock distributed shared
+        // memory would take longer)
+        float* dst = p.ws_o + cm_slot(t, half, split) * kCmRowFloats * 64 + (h & 63) * kDvHalf +
+                     128 * c + 32 * cc;
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<float4*>(st_s + h * 1024 + (((8 * c + v) ^ (h & 31)) << 4)) =
+          __stcg(reinterpret_cast<float4*>(dst + 4 * v),
+                 make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                             __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv));
+      } else {  // fp32 rows of 1 KiB: chunks 32c + 8cc .. +7
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          *reinterpret_cast<float4*>(st_s + h * 1024 + (((32 * c + 8 * cc + v) ^ (h & 31)) << 4)) =
               make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
                           __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
       }
     }
-    if (p.splits == 1) {
-      if (half == 0 && h < p.H && p.lse) p.lse[(size_t)t * p.H + h] = lse2 * 0.69314718055994531f;
-    } else if (p.cluster_merge) {
-      reinterpret_cast<float*>(smem + Layout::rowmax)[h] = lse2;  // the tile maxima are done
-      fence_proxy_async_smem();  // the staged rows and lse are read by a bulk copy
-    } else {
-      const size_t unit = ((size_t)t * 2 + half) * p.splits + split;
-      __stcg(p.ws_lse + unit * kHeads + h, lse2);
+    if (team == 0) {
+      if (p.splits == 1) {
+        if (half == 0 && h < p.H && p.lse) p.lse[(size_t)t * p.H + h] = lse2 * 0.69314718055994531f;
+      } else if (!p.cluster_merge) {
+        const size_t unit = ((size_t)t * 2 + half) * p.splits + split;
+        __stcg(p.ws_lse + unit * kHeads + h, lse2);
+      } else if ((h >> 6) != split) {
+        __stcg(p.ws_lse + cm_slot(t, half, split) * 64 + (h & 63), lse2);
+      }
     }
   }
   tc_fence_before();
@@ -709,51 +840,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   if (p.cluster_merge) {
-    // Split s of this half finalises heads [64s, 64s + 64): it sends the other split the staged
-    // rows of that split's heads and their lse, receives its own in the (idle) exchange and P
-    // buffers and the row-maximum area, and combines the two normalised partials by their lse.
-    const int h0 = 64 * split, ph0 = 64 * (split ^ 1);
-    const uint32_t speer = crank ^ 2u;
-    const uint32_t rbar = map_cluster(&ctl->mrg, speer);
-    if (tid == 0) {
-      bulk_copy_to_cluster(map_cluster(smem + Layout::xbuf, speer), st_s + ph0 * 1024, 64 * 1024, rbar);
-      bulk_copy_to_cluster(map_cluster(smem + Layout::rowmax + 128 * 4, speer),
-                           smem + Layout::rowmax + ph0 * 4, 64 * 4, rbar);
-      bulk_commit();
-    }
-    const bool ok = mbar_wait<true>(&ctl->mrg, 0, abort, p.status);
-    const float* lse_own = reinterpret_cast<const float*>(smem + Layout::rowmax);
-    const float* lse_oth = lse_own + 128;  // indexed by head - h0
-    if (ok) {
-#pragma unroll 2
-      for (int item = tid; item < 64 * 64; item += kThreads) {
-        const int hr = item >> 6, c = item & 63, h = h0 + hr;
-        const float lo = lse_own[h], lp = lse_oth[hr];
-        const float M = fmaxf(lo, lp);
-        const float wo = lo == -INFINITY ? 0.f : exp2f(lo - M);
-        const float wp = lp == -INFINITY ? 0.f : exp2f(lp - M);
-        const float W = wo + wp, inv = W > 0.f ? 1.f / W : 0.f;
-        const uint32_t sw = (uint32_t)((c ^ (h & 31)) << 4);
-        const float4 a = *reinterpret_cast<const float4*>(st_s + h * 1024 + sw);
-        const float4 o = *reinterpret_cast<const float4*>(smem + Layout::xbuf + hr * 1024 + sw);
-        // split 0's term first in both CTAs
-        const float4 x0 = split == 0 ? a : o, x1 = split == 0 ? o : a;
-        const float w0 = (split == 0 ? wo : wp) * inv, w1 = (split == 0 ? wp : wo) * inv;
-        if (h < p.H) {
-          uint2 v;
-          v.x = pack_bf16(w0 * x0.x + w1 * x1.x, w0 * x0.y + w1 * x1.y);
-          v.y = pack_bf16(w0 * x0.z + w1 * x1.z, w0 * x0.w + w1 * x1.w);
-          *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf + c * 4) = v;
-        }
-      }
-      if (half == 0 && tid < 64 && h0 + tid < p.H && p.lse) {
-        const float lo = lse_own[h0 + tid], lp = lse_oth[tid];
-        const float M = fmaxf(lo, lp);
-        const float W = (lo == -INFINITY ? 0.f : exp2f(lo - M)) + (lp == -INFINITY ? 0.f : exp2f(lp - M));
+    // Split s of this half finalises heads [64s, 64s + 64): its own rows of them are staged in
+    // the ring, the other split's are in that split's workspace slot (written before the cluster
+    // barrier, whose release/acquire orders them before these loads); the two normalised
+    // partials combine by their lse, split 0's term first.
+    const int h0 = 64 * split;
+    const size_t oth = cm_slot(t, half, split ^ 1);
+    float* w0s = reinterpret_cast<float*>(smem + Layout::xbuf);  // idle now: [64] and [64]
+    float* w1s = w0s + 64;
+    if (tid < 64) {
+      const float lo = lsebuf[h0 + tid], lp = __ldcg(p.ws_lse + oth * 64 + tid);
+      const float M = fmaxf(lo, lp);
+      const float wo = lo == -INFINITY ? 0.f : exp2f(lo - M);
+      const float wp = lp == -INFINITY ? 0.f : exp2f(lp - M);
+      const float W = wo + wp, inv = W > 0.f ? 1.f / W : 0.f;
+      w0s[tid] = (split == 0 ? wo : wp) * inv;
+      w1s[tid] = (split == 0 ? wp : wo) * inv;
+      if (half == 0 && h0 + tid < p.H && p.lse)
         p.lse[(size_t)t * p.H + h0 + tid] = W > 0.f ? (M + log2f(W)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+    // thread -> (4 value columns, 8 heads): a warp reads 512 contiguous bytes of a row per load,
+    // all eight loads of a thread in flight together
+    const float* src = p.ws_o + oth * kCmRowFloats * 64;
+    const int c = tid & 63, hb = tid >> 6;
+    float4 ov[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ov[k] = __ldcg(reinterpret_cast<const float4*>(src + (hb + 8 * k) * kDvHalf + 4 * c));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int hr = hb + 8 * k, h = h0 + hr;
+      const float4 a = *reinterpret_cast<const float4*>(st_s + h * 1024 + ((c ^ (h & 31)) << 4));
+      const float4 x0 = split == 0 ? a : ov[k], x1 = split == 0 ? ov[k] : a;
+      const float w0 = w0s[hr], w1 = w1s[hr];
+      if (h < p.H) {
+        uint2 v;
+        v.x = pack_bf16(w0 * x0.x + w1 * x1.x, w0 * x0.y + w1 * x1.y);
+        v.y = pack_bf16(w0 * x0.z + w1 * x1.z, w0 * x0.w + w1 * x1.w);
+        *reinterpret_cast<uint2*>(p.out + ((size_t)t * p.H + h) * kDv + half * kDvHalf + 4 * c) = v;
       }
     }
-    if (tid == 0) bulk_wait_read_all();  // the outgoing copy has read its source
     return;
   }
   {
@@ -773,11 +900,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     __threadfence();
     const int prev = atomicAdd(&p.ws_count[t * 2 + half], 1);
-    ctl->last = prev == p.splits - 1;
-    if (ctl->last) p.ws_count[t * 2 + half] = 0;  // ready for the next call
+    ctl->nvalid = prev == p.splits - 1;
+    if (ctl->nvalid) p.ws_count[t * 2 + half] = 0;  // ready for the next call
   }
   __syncthreads();
-  if (!ctl->last) return;
+  if (!ctl->nvalid) return;
   __threadfence();
   const size_t unit0 = ((size_t)t * 2 + half) * p.splits;
   // Coalesced merge: thread -> (4 value columns c4, heads h0 + 8k); a warp reads 512 contiguous
@@ -842,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct Plan {
   int splits, rows_per;
-  bool cluster_merge;  // two splits merged through distributed shared memory (cluster of 4)
+  bool cluster_merge;  // two splits of a token in one cluster of 4, merged through the workspace
 };
 
 static Plan plan(const dsa_sfa_args& a, bool prefill, int sm_count) {
@@ -867,11 +994,16 @@ static Plan plan(const dsa_sfa_args& a, bool prefill, int sm_count) {
   return pl;
 }
 
+// Workspace: [units][rows][256] fp32 partial rows, then [units][rows] lse, then n_q * 2 arrival
+// counters (used with three or more splits; zero between calls).  Three or more splits: a unit is
+// (token, value half, split) with all 128 rows; two splits (cluster merge): 64 rows, those of the
+// heads the other split finalises.
 static size_t ws_bytes(const dsa_sfa_args& a, const Plan& pl) {
-  if (pl.splits <= 1 || pl.cluster_merge) return 0;
+  if (pl.splits <= 1) return 0;
   const size_t units = (size_t)a.n_q * 2 * pl.splits;
-  size_t bytes = units * kHeads * kDvHalf * 4;   // partial o
-  bytes += units * kHeads * 4;                    // partial lse
+  const size_t rows = pl.cluster_merge ? 64 : kHeads;
+  size_t bytes = units * rows * kDvHalf * 4;     // partial o
+  bytes += units * rows * 4;                      // partial lse
   bytes = (bytes + 255) / 256 * 256;
   bytes += (size_t)a.n_q * 2 * 4;                 // counters
   return (bytes + 255) / 256 * 256;
@@ -922,10 +1054,11 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
 #endif
   if (need > 0) {
     const size_t units = (size_t)a.n_q * 2 * pl.splits;
+    const size_t rows = pl.cluster_merge ? 64 : kHeads;
     uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);
     p.ws_o = reinterpret_cast<float*>(ws);
-    p.ws_lse = reinterpret_cast<float*>(ws + units * kHeads * kDvHalf * 4);
-    const size_t cnt_off = ((units * kHeads * kDvHalf * 4 + units * kHeads * 4) + 255) / 256 * 256;
+    p.ws_lse = reinterpret_cast<float*>(ws + units * rows * kDvHalf * 4);
+    const size_t cnt_off = ((units * rows * kDvHalf * 4 + units * rows * 4) + 255) / 256 * 256;
     p.ws_count = reinterpret_cast<int*>(ws + cnt_off);
   } else {
     p.ws_o = nullptr;

@@ -133,10 +133,10 @@ dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
  * device check failure: the row is skipped and *status set.
  *
  * dsa_sfa_decode targets few tokens per sequence: it splits each token's K rows over several CTA
- * pairs and merges the partial softmax states, on chip when there are two splits (the usual
- * case; no workspace) and in `workspace` when there are more; dsa_sfa_prefill targets many
- * tokens per sequence (one token per CTA pair, no workspace).  Both give the same result up to
- * fp32 rounding.
+ * pairs and merges the partial softmax states through `workspace` (dsa_sfa_workspace_bytes()
+ * bytes; with two splits, the usual case, each split finalises half of the heads);
+ * dsa_sfa_prefill targets many tokens per sequence (one token per CTA pair, no workspace).  Both
+ * give the same result up to fp32 rounding.
  *
  * Stream order: both are launched as programmatic dependents of the preceding kernel in the
  * stream, so their CTAs may start (barrier set-up, tensor-memory allocation) while that kernel

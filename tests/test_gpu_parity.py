@@ -110,8 +110,8 @@ def test_prefill_small(cuda_lib):
 
 @pytest.mark.parametrize("splits", [2, 4])
 def test_integer_config_row_splits_16_heads(cuda_lib, splits):
-    """16 SFA heads (padded to 128 on chip) through the on-chip merge of two splits and the
-    workspace merge of four, on the integer-exact indexer config."""
+    """16 SFA heads (padded to 128 on chip) through the cluster merge of two splits and the
+    last-CTA merge of four, on the integer-exact indexer config."""
     inp_cpu, inp = _small("decode_int_4k", seq_lens=[4096, 700], n_new=[1, 2])
     g = run_gpu(inp, prefill=False, row_splits=splits)
     assert g["status"] == 0
@@ -123,9 +123,9 @@ def test_integer_config_row_splits_16_heads(cuda_lib, splits):
 
 @pytest.mark.parametrize("splits", [1, 2, 3])
 def test_decode_row_split_counts(cuda_lib, splits):
-    """One split (no merge), two (the splits of a token merge through distributed shared memory
-    in a cluster of four) and three (partials merged through the workspace) give the oracle's
-    attention on the same index sets."""
+    """One split (no merge), two (the splits of a token share a cluster of four and each finalises
+    half of the heads) and three (the last CTA merges all partials) give the oracle's attention
+    on the same index sets."""
     inp_cpu, inp = _small("decode_32k", seq_lens=[5000, 3000, 129], n_new=[1, 2, 1])
     g = run_gpu(inp, prefill=False, row_splits=splits)
     assert g["status"] == 0
