@@ -227,6 +227,13 @@ DSA_DEV void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, 
       : "memory");
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+DSA_DEV void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+
 // Four rows (y0..y3) of one column box (x) of a 2-D map whose box is one row high.
 DSA_DEV void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y0, int y1,
                          int y2, int y3) {

@@ -846,6 +846,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // partials combine by their lse, split 0's term first.
     const int h0 = 64 * split;
     const size_t oth = cm_slot(t, half, split ^ 1);
+    // thread -> (4 value columns, 8 heads): a warp reads 512 contiguous bytes of a row per load;
+    // all eight loads of a thread and the lse loads below are in flight together
+    const float* src = p.ws_o + oth * kCmRowFloats * 64;
+    const int c = tid & 63, hb = tid >> 6;
+    float4 ov[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ov[k] = __ldcg(reinterpret_cast<const float4*>(src + (hb + 8 * k) * kDvHalf + 4 * c));
     float* w0s = reinterpret_cast<float*>(smem + Layout::xbuf);  // idle now: [64] and [64]
     float* w1s = w0s + 64;
     if (tid < 64) {
@@ -860,14 +868,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[(size_t)t * p.H + h0 + tid] = W > 0.f ? (M + log2f(W)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
-    // thread -> (4 value columns, 8 heads): a warp reads 512 contiguous bytes of a row per load,
-    // all eight loads of a thread in flight together
-    const float* src = p.ws_o + oth * kCmRowFloats * 64;
-    const int c = tid & 63, hb = tid >> 6;
-    float4 ov[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      ov[k] = __ldcg(reinterpret_cast<const float4*>(src + (hb + 8 * k) * kDvHalf + 4 * c));
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int hr = hb + 8 * k, h = h0 + hr;
