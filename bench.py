@@ -124,12 +124,20 @@ class ClockSampler:
             self._stop.set()
             self._t.join()
 
+    def mark(self):
+        """Record how many samples the first window (the timed region) holds."""
+        self.n_first = len(self.samples)
+
     def summary(self):
         if not self.ok or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"]}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "samples": len(self.samples),
-                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b]}
+        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+               "samples": len(self.samples),
+               "reasons": [n for b, n in self.REASONS.items() if self.reasons & b]}
+        if getattr(self, "n_first", None) is not None:
+            out["samples_timed_region"] = self.n_first
+            out["window"] = "timed region + per-kernel passes"
+        return out
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -325,29 +333,33 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(pci) as clk:
+    # the clock sampler runs through the timed region and the per-kernel passes after it (a
+    # timed region of a few ms would otherwise hold one or two NVML samples)
+    clk = ClockSampler(pci)
+    with clk:
         with torch.cuda.stream(stream):
             e_all[0].record(stream)
             for i in range(K):
                 step(i)
             e_all[1].record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = e_all[0].elapsed_time(e_all[1])
-    if int(status.item()) != 0:
-        raise RuntimeError("device status %d in the timed region" % int(status.item()))
-    t = torch.tensor([total_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
-    value = n_q * world * K / (total_ms / 1000.0)
+        clk.mark()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = e_all[0].elapsed_time(e_all[1])
+        if int(status.item()) != 0:
+            raise RuntimeError("device status %d in the timed region" % int(status.item()))
+        t = torch.tensor([total_ms], device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+        value = n_q * world * K / (total_ms / 1000.0)
 
-    # ---- per-kernel durations: each entry point alone, its own event-bracketed pass of
-    # args.kernel_reps launches (independent of --steps), median
-    NK = max(50, args.kernel_reps)
-    li_ms = _median_launch_ms(lib, lib.dsa_li_topk, li_args, sp, stream, NK)
-    sfa_ms = _median_launch_ms(lib, sfa_entry, sfa_args, sp, stream, NK)
+        # ---- per-kernel durations: each entry point alone, its own event-bracketed pass of
+        # args.kernel_reps launches (independent of --steps), median
+        NK = max(50, args.kernel_reps)
+        li_ms = _median_launch_ms(lib, lib.dsa_li_topk, li_args, sp, stream, NK)
+        sfa_ms = _median_launch_ms(lib, sfa_entry, sfa_args, sp, stream, NK)
     if int(status.item()) != 0:
         raise RuntimeError("device status %d in the per-kernel passes" % int(status.item()))
 

@@ -41,9 +41,11 @@
 //   - O (128 x 256 fp32 = half of TMEM) accumulates P.V_r across tiles.
 // Each head's 128x512 fp32 O would fill all of TMEM, hence the value split over the pair; the
 // split of the Q.K^T dimensions halves both the gathered bytes and the tensor work of each CTA.
-// With two row splits both pairs of a token form one cluster of four and merge their normalised
-// partials through distributed shared memory; with more, the partial (o, lse) go to the
-// caller's workspace and the last CTA of a (token, r) to finish merges them.
+// With two row splits both pairs of a token form one cluster of four: split s finalises heads
+// [64s, 64s + 64) of its value half, the other split writes its normalised rows of those heads
+// and their lse to the caller's workspace (L2) before the cluster barrier, and split s combines
+// them with its own after it.  With more splits the partial (o, lse) go to the workspace and the
+// last CTA of a (token, r) to finish merges them.
 //
 // FP8 latent cache ("Inference Optimization for Kimi K3.1 Pro", section 4: the cache stored in
 // FP8 per token and 128-column tile, the attention arithmetic in BF16): rows of 576 e4m3 codes

@@ -177,7 +177,9 @@ typedef struct {
                                 it beyond fp32 rounding); ignored by dsa_sfa_prefill        */
 } dsa_sfa_args;
 
-/* Scratch that dsa_sfa_decode needs for these arguments (0 if none).  Host only, no CUDA. */
+/* Scratch that dsa_sfa_decode needs for these arguments (0 if none).  Host only: it reads the
+ * current device's SM count (the split plan depends on it; 152 when no device is visible) and
+ * launches nothing.  Only n_q, H, K and row_splits are read. */
 size_t dsa_sfa_workspace_bytes(const dsa_sfa_args* args);
 
 dsa_status dsa_sfa_decode(const dsa_sfa_args* args, dsa_stream_t stream);
@@ -199,6 +201,11 @@ dsa_status dsa_sfa_prefill(const dsa_sfa_args* args, dsa_stream_t stream);
  *  - All calls on a device share the one array, which keeps the last call's contents; the call
  *    clears what must start at zero.  Calls whose work overlaps on the GPU (other streams, other
  *    host threads) race on the array: serialise them.
+ *  - Capacity: with row_splits = 0 and K <= 2048 the library never plans more CTA pairs than
+ *    one wave holds (2 * n_q * splits <= SMs), and a plan needs at most
+ *    n_q * splits * 263,168 bytes (+ 512 for alignment and counters), so 20 MiB covers every such
+ *    plan on a GPU of 159 SMs or fewer (152 on GB300).  An explicit row_splits or a larger K can
+ *    exceed it; such calls are rejected as above.
  */
 #define DSA_SFA_STATIC_SCRATCH_BYTES (20u * 1024u * 1024u)
 dsa_status dsa_sfa_decode_static(const dsa_sfa_args* args, dsa_stream_t stream);

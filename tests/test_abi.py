@@ -43,6 +43,22 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(dsa.PrologArgs) == 10 * 4 + 2 * 4 + 16 * 8 + 8 + 8
 
 
+def test_static_scratch_covers_every_automatic_decode_plan():
+    """20 MiB of static scratch holds the split-merge workspace of every decode plan the library
+    chooses by itself (row_splits = 0) for K <= 2048, at the SM count the plan sees here (the
+    152-SM default without a GPU); an explicit row_splits may exceed it."""
+    worst = 0
+    for n_q in list(range(1, 161)) + [256, 1024]:
+        q = torch.empty((n_q, 128, 576), dtype=torch.bfloat16, device="meta")
+        for K in (1, 63, 64, 65, 128, 500, 1000, 1024, 2047, 2048):
+            idx = torch.empty((n_q, K), dtype=torch.int32, device="meta")
+            worst = max(worst, dsa.sfa_workspace_bytes(q, idx))
+    assert 0 < worst <= dsa.SFA_STATIC_SCRATCH_BYTES
+    q = torch.empty((32, 128, 576), dtype=torch.bfloat16, device="meta")
+    idx = torch.empty((32, 2048), dtype=torch.int32, device="meta")
+    assert dsa.sfa_workspace_bytes(q, idx, row_splits=32) > dsa.SFA_STATIC_SCRATCH_BYTES
+
+
 def test_page_bytes():
     assert dsa.page_bytes(dsa.DSA_BF16, 64, 576) == 64 * 576 * 2
     assert dsa.page_bytes(dsa.DSA_FP8_E4M3, 64, 128) == 64 * 128
