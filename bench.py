@@ -284,6 +284,8 @@ def run_ours(args):
     kv = base["kv8_pool"] if wl.kv_dtype == "fp8" else base["kv_pool"]
     ws = None if prefill else dsa.new_workspace(
         dsa.sfa_workspace_bytes(base["q_sfa"], torch.empty((n_q, wl.K), dtype=torch.int32)), dev)
+    li_nb = dsa.li_workspace_bytes(len(wl.seq_lens), wl.K, ms, mq)  # sequences split into units
+    li_ws = torch.empty((li_nb,), dtype=torch.uint8, device=dev) if li_nb else None
     bufs, li_args, sfa_args = [], [], []
     for inp in sets:
         o = {"idx": torch.empty((n_q, wl.K), dtype=torch.int32, device=dev),
@@ -295,7 +297,7 @@ def run_ours(args):
             inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"], inp["q_start"],
             wl.K, q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"), max_seq_len=ms,
             max_q_per_seq=mq, out_idx=o["idx"], out_cnt=o["cnt"], status=status,
-            q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf")))
+            q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf"), workspace=li_ws))
         sfa_args.append(dsa.sfa_args(
             inp["q_sfa"], kv, inp["pt_kv"], inp["seq_lens"], inp["q_start"], o["idx"],
             softmax_scale=wl.softmax_scale, max_seq_len=ms, max_q_per_seq=mq, out=o["out"],
@@ -400,7 +402,8 @@ def run_ours(args):
         li2 = [dsa.li_topk_args(d["q_li"], d["w"], base["k_pool"], d["pt_k"], d["seq_lens"], d["q_start"],
                                 wl.K, q_scale=d.get("q_scale"), k_scale=base.get("k_scale"),
                                 max_seq_len=ms, max_q_per_seq=mq, out_idx=o["idx"], out_cnt=o["cnt"],
-                                status=status, q_sf=d.get("q_sf"), k_sf=base.get("k_sf"))
+                                status=status, q_sf=d.get("q_sf"), k_sf=base.get("k_sf"),
+                                workspace=li_ws)
                for d, o in zip(din, dout)]
         sfa2 = [dsa.sfa_args(d["q_sfa"], kv, d["pt_kv"], d["seq_lens"], d["q_start"], o["idx"],
                              softmax_scale=wl.softmax_scale, max_seq_len=ms, max_q_per_seq=mq,
@@ -499,7 +502,7 @@ def run_ours(args):
         "step_hbm": {"metric_bytes": work["metric_bytes"], "achieved_gbs": step_gbs,
                      "frac": step_gbs / hbm, "peak_kind": peak_kind},
         "kernels": kernels,
-        "gpu_launches": 2 * K,
+        "gpu_launches": (3 if li_nb else 2) * K,  # indexer (+ unit merge) + attention per step
         "clocks": clk.summary(),
     }
     if e2e:

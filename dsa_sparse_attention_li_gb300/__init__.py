@@ -30,7 +30,7 @@ HOOKS_LIB_PATH = os.path.join(_PKG, "libdsa_testhooks.so")
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_DEVICE_CHECK, DSA_ERR_TIMEOUT = range(6)
 DSA_BF16, DSA_FP8_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2
 
-SYMBOLS = ["dsa_status_string", "dsa_last_error", "dsa_abi_version", "dsa_li_topk",
+SYMBOLS = ["dsa_status_string", "dsa_last_error", "dsa_abi_version", "dsa_li_workspace_bytes", "dsa_li_topk",
            "dsa_sfa_workspace_bytes", "dsa_sfa_decode", "dsa_sfa_prefill",
            "dsa_sfa_decode_static", "dsa_page_bytes", "dsa_page_table_validate",
            "dsa_cache_write", "dsa_prolog_workspace_bytes", "dsa_indexer_prolog", "dsa_topk_merge"]
@@ -51,7 +51,8 @@ class LiArgs(ctypes.Structure):
         "B", "n_q", "H_I", "d_I", "K", "page_size", "max_pages", "num_pages", "max_seq_len",
         "max_q_per_seq", "dtype")] + [(n, ctypes.c_void_p) for n in (
             "q", "q_scale", "w", "k_pool", "k_scale", "page_table", "seq_lens", "q_start",
-            "out_idx", "out_cnt", "status", "q_sf", "k_sf", "out_score")]
+            "out_idx", "out_cnt", "status", "q_sf", "k_sf", "out_score", "workspace")] + [
+        ("workspace_bytes", ctypes.c_size_t)]
 
 
 class MergeArgs(ctypes.Structure):
@@ -120,6 +121,8 @@ def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.dsa_abi_version.restype = ctypes.c_int
     lib.dsa_li_topk.argtypes = [ctypes.POINTER(LiArgs), P]
     lib.dsa_li_topk.restype = ctypes.c_int
+    lib.dsa_li_workspace_bytes.argtypes = [ctypes.POINTER(LiArgs)]
+    lib.dsa_li_workspace_bytes.restype = ctypes.c_size_t
     for f in (lib.dsa_sfa_decode, lib.dsa_sfa_prefill, lib.dsa_sfa_decode_static):
         f.argtypes = [ctypes.POINTER(SfaArgs), P]
         f.restype = ctypes.c_int
@@ -187,9 +190,10 @@ def _host_max(seq_lens: torch.Tensor, q_start: torch.Tensor, max_seq_len, max_q_
 
 def li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_scale=None,
                  max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None,
-                 q_sf=None, k_sf=None, out_score=None):
+                 q_sf=None, k_sf=None, out_score=None, workspace=None):
     """Fill the C argument struct of dsa_li_topk (tensors must outlive the call).  e4m3 q/k take
-    either fp32 q_scale/k_scale (FP8) or uint8 E8M0 group scales q_sf/k_sf (MXFP8)."""
+    either fp32 q_scale/k_scale (FP8) or uint8 E8M0 group scales q_sf/k_sf (MXFP8);
+    ``workspace`` holds li_workspace_bytes() bytes when that is not 0."""
     fp8 = q.dtype == torch.float8_e4m3fn
     n_q, H_I, d_I = q.shape
     max_seq_len, max_q_per_seq = _host_max(seq_lens, q_start, max_seq_len, max_q_per_seq)
@@ -206,24 +210,39 @@ def li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None
     a.out_idx, a.out_cnt, a.status = _ptr(out_idx), _ptr(out_cnt), _ptr(status)
     a.q_sf, a.k_sf = _ptr(q_sf), _ptr(k_sf)
     a.out_score = _ptr(out_score)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return a
+
+
+def li_workspace_bytes(B: int, K: int, max_seq_len: int, max_q_per_seq: int) -> int:
+    """Scratch bytes dsa_li_topk needs for a batch of this shape (0: none)."""
+    a = LiArgs()
+    a.B, a.K, a.max_seq_len, a.max_q_per_seq = int(B), int(K), int(max_seq_len), int(max_q_per_seq)
+    return int(load().dsa_li_workspace_bytes(ctypes.byref(a)))
 
 
 def li_topk(q, w, k_pool, page_table, seq_lens, q_start, K, *, q_scale=None, k_scale=None,
             max_seq_len=None, max_q_per_seq=None, out_idx=None, out_cnt=None, status=None,
-            stream=None, q_sf=None, k_sf=None, out_score=None):
+            stream=None, q_sf=None, k_sf=None, out_score=None, workspace=None):
     """Fused indexer scoring + top-K.  Returns (idx [n_q, K] int32, cnt [n_q] int32); with
-    ``out_score`` ([n_q, K] fp32) also the score of every selected position."""
+    ``out_score`` ([n_q, K] fp32) also the score of every selected position.  The scratch for
+    sequences split into position units is allocated here unless ``workspace`` is given."""
     lib = load()
     n_q = q.shape[0]
     if out_idx is None:
         out_idx = torch.empty((n_q, K), dtype=torch.int32, device=q.device)
     if out_cnt is None:
         out_cnt = torch.empty((n_q,), dtype=torch.int32, device=q.device)
+    max_seq_len, max_q_per_seq = _host_max(seq_lens, q_start, max_seq_len, max_q_per_seq)
+    if workspace is None:
+        nbytes = li_workspace_bytes(seq_lens.shape[0], K, max_seq_len, max_q_per_seq)
+        if nbytes:
+            workspace = torch.empty((nbytes,), dtype=torch.uint8, device=q.device)
     a = li_topk_args(q, w, k_pool, page_table, seq_lens, q_start, K, q_scale=q_scale,
                      k_scale=k_scale, max_seq_len=max_seq_len, max_q_per_seq=max_q_per_seq,
                      out_idx=out_idx, out_cnt=out_cnt, status=status, q_sf=q_sf, k_sf=k_sf,
-                     out_score=out_score)
+                     out_score=out_score, workspace=workspace)
     _check(lib.dsa_li_topk(ctypes.byref(a), _stream(stream)), "dsa_li_topk")
     return out_idx, out_cnt
 
@@ -410,7 +429,7 @@ def indexer_prolog(inp: dict, *, q_out=None, q_sf=None, w_out=None, workspace=No
 
 def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=None, status=None,
                 stream=None, max_seq_len=None, max_q_per_seq=None, prefill: bool = False,
-                row_splits: int = 0):
+                row_splits: int = 0, li_workspace=None):
     """One pass of the whole hot path over a batch laid out as ``dsa_inputs.generate`` does:
     li_topk followed by sfa_decode (or sfa_prefill) on the same stream."""
     wl = inp["wl"]
@@ -419,7 +438,8 @@ def decode_step(inp: dict, *, idx=None, cnt=None, out=None, lse=None, workspace=
     idx, cnt = li_topk(inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"],
                        inp["q_start"], wl.K, q_scale=inp.get("q_scale"), k_scale=inp.get("k_scale"),
                        max_seq_len=ms, max_q_per_seq=mq, out_idx=idx, out_cnt=cnt, status=status,
-                       stream=stream, q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf"))
+                       stream=stream, q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf"),
+                       workspace=li_workspace)
     f = sfa_prefill if prefill else sfa_decode
     kv = inp["kv8_pool"] if getattr(wl, "kv_dtype", "bf16") == "fp8" else inp["kv_pool"]
     out, lse = f(inp["q_sfa"], kv, inp["pt_kv"], inp["seq_lens"], inp["q_start"], idx,

@@ -174,10 +174,17 @@ dsa_status dsa_li_topk(const dsa_li_args* a, dsa_stream_t stream) {
   if (a->page_size != 64) return fail(DSA_ERR_UNSUPPORTED, "li_topk: page_size must be 64");
   if (a->K > 2048) return fail(DSA_ERR_UNSUPPORTED, "li_topk: K > 2048");
   if (a->max_seq_len > 131072) return fail(DSA_ERR_UNSUPPORTED, "li_topk: max_seq_len > 131072");
+  if (a->workspace != nullptr && (reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+    return fail(DSA_ERR_INVALID_ARG, "li_topk: workspace must be 256-byte aligned");
   std::string err;
   const dsa_status s = dsa::launch_li_topk(*a, reinterpret_cast<cudaStream_t>(stream), err);
   if (s != DSA_OK) g_last_error = err;
   return s;
+}
+
+size_t dsa_li_workspace_bytes(const dsa_li_args* a) {
+  if (!a || a->B <= 0 || a->K <= 0 || a->max_seq_len <= 0 || a->max_q_per_seq <= 0) return 0;
+  return dsa::li_workspace_bytes(*a);
 }
 
 static dsa_status sfa_common(const dsa_sfa_args* a, bool prefill, dsa_stream_t stream) {

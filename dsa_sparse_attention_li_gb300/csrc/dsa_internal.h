@@ -16,6 +16,25 @@ dsa_status launch_sfa(const dsa_sfa_args& a, bool prefill, cudaStream_t stream, 
 size_t sfa_workspace_bytes(const dsa_sfa_args& a);
 dsa_status launch_prolog(const dsa_prolog_args& a, cudaStream_t stream, std::string& err);
 dsa_status launch_topk_merge(const dsa_topk_merge_args& a, cudaStream_t stream, std::string& err);
+
+// Indexer over position units: workspace bytes dsa_li_topk needs (0 when no sequence is split).
+size_t li_workspace_bytes(const dsa_li_args& a);
+// Merge of the units' top-K candidates of every token whose sequence was split (merge.cu): unit u
+// of token group g of sequence b left its candidates of token tt at slot
+// ((b * groups + g) * units + u) * T + tt of cand_idx / cand_score ([slots][K]).
+struct UnitMergeArgs {
+  int B, n_q, K, T, groups, units;
+  int span;       // positions a cluster covers: a sequence of L positions has ceil(L / span) units
+  int max_pages;  // (the indexer's validity bound on L)
+  const int* seq_lens;
+  const int* q_start;
+  int* cand_idx;
+  float* cand_score;
+  int* out_idx;
+  int* out_cnt;
+  float* out_score;
+};
+dsa_status launch_unit_merge(const UnitMergeArgs& a, cudaStream_t stream, std::string& err);
 size_t prolog_workspace_bytes(const dsa_prolog_args& a);
 dsa_status launch_cache_write(void* pool, float* scale_pool, int num_pages, int page_size, int dim,
                               int elem_bytes, const int32_t* page_table, int max_pages, int B,

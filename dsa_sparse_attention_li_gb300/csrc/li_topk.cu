@@ -47,12 +47,17 @@ constexpr int kTileKeys = 128;
 constexpr int kHistWords = 1024;  // 2048 radix bins, two 16-bit counters per 32-bit word
 constexpr int kMaxCluster = 16;
 constexpr int kCtlBytes = 2560;   // shared control block (mbarriers, counters), sizeof(Ctl) rounded up
+// Sequences longer than kUnitSpan positions (decode and two-token groups) are split into units
+// of at most one cluster's span; the unit merge sorts units x K candidates in shared memory.
+constexpr int kUnitSpan = 32768;
+constexpr int kMaxUnitCand = 16384;
 
 struct Params {
   int B, n_q, K, max_pages, num_pages;
   int groups;  // token groups per sequence
-  int chunk;   // key positions per CTA (multiple of 128)
+  int chunk;   // key positions per CTA at most (multiple of 128; sizes the shared memory)
   int C;       // cluster size
+  int units;   // position units per sequence at most (1: one cluster covers a whole sequence)
   int nstage;  // TMA ring depth
   const float* w;
   const float* q_scale;
@@ -66,6 +71,12 @@ struct Params {
   const uint8_t* q_sf;  // MXFP8: E8M0 scales of 32-element groups, [n_q][H_I][D_I/32]
   const uint8_t* k_sf;  //        and [num_pages][64][D_I/32]
   float* out_score;     // optional [n_q][K]: the score of every emitted position (-inf padding)
+  // units > 1: a sequence of more than C * chunk positions is split into equal units of at most
+  // C * chunk positions, one cluster each; such a unit writes its own top-K (ascending
+  // positions, -1 padding) and their scores to slot ((b * groups + g) * units + u) * T + tt of
+  // these [slots][K] arrays, and the unit merge selects the token's top-K from them
+  int* cand_idx;
+  float* cand_score;
 #ifdef DSA_TEST_HOOKS
   int stall;            // test build: CTA 0's MMA thread waits on a barrier nothing arrives on
 #endif
@@ -258,28 +269,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)cluster_rank();
+  // Clusters in launch order take the highest units first (only long sequences have them, and
+  // they are full), each sequence's first unit last (short sequences are a single unit): the
+  // longest work starts first.
   const int cl = blockIdx.x / p.C;
-  const int b = cl / p.groups, g = cl % p.groups;
+  const int nbg = p.B * p.groups;
+  const int unit = p.units - 1 - cl / nbg;  // position unit of the sequence
+  const int b = cl % nbg / p.groups, g = cl % nbg % p.groups;
   if (b >= p.B) return;
   const int qs = p.q_start[b];
   const int n_b = p.q_start[b + 1] - qs;
   const int L = p.seq_lens[b];
   // Cluster-uniform validity (every CTA of the cluster reads the same values).
-  if (g == p.groups - 1 && rank == 0 && tid == 0 && n_b > p.groups * T)
+  if (unit == 0 && g == p.groups - 1 && rank == 0 && tid == 0 && n_b > p.groups * T)
     report(p.status, kStatusDeviceCheck);
-  if (n_b < 0 || L < n_b || L > p.C * p.chunk || L > p.max_pages * 64 || qs < 0 ||
+  if (n_b < 0 || L < n_b || L > p.units * p.C * p.chunk || L > p.max_pages * 64 || qs < 0 ||
       qs + n_b > p.n_q) {
-    if (rank == 0 && tid == 0) report(p.status, kStatusDeviceCheck);
+    if (unit == 0 && rank == 0 && tid == 0) report(p.status, kStatusDeviceCheck);
     return;
   }
   const int nt = min(T, n_b - g * T);
   if (nt <= 0) return;
+  // The sequence's units (one unless it is longer than C * chunk) are equal, and within a unit
+  // each CTA owns an equal multiple of 128 positions, so short sequences spread over every CTA
+  // of their cluster instead of filling the first ones.
+  const int n_u = p.units == 1 ? 1 : max(1, (L + p.C * p.chunk - 1) / (p.C * p.chunk));
+  if (unit >= n_u) return;
+  const int span_u = (L + n_u - 1) / n_u;
+  const int chunk = max(kTileKeys, ((span_u + p.C - 1) / p.C + kTileKeys - 1) / kTileKeys * kTileKeys);
+  const int u_lo = unit * p.C * chunk;              // the unit's positions: [u_lo, u_hi)
+  const int u_hi = min(L, u_lo + p.C * chunk);
+  const bool direct = n_u == 1;                     // writes the token's final top-K
   const int t0 = qs + g * T;
   const int pos0 = L - n_b + g * T;  // position of token t0
-  const int lo = rank * p.chunk;
-  const int hi = min(lo + p.chunk, pos0 + nt);
+  const int lo = u_lo + rank * chunk;
+  const int lim = min(lo + chunk, u_hi);            // this CTA's positions: [lo, lim)
+  const int hi = min(lim, pos0 + nt);
   const int ntile = hi > lo ? (hi - lo + kTileKeys - 1) / kTileKeys : 0;
-  const int nscan = min(ntile * kTileKeys, p.chunk);
+  const int nscan = min(ntile * kTileKeys, chunk);
   const int npages_seq = (L + 63) / 64;
 
   // ---------------- setup
@@ -493,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             s = a0 + a1;
           }
           if (FP8 && !MX) s *= ks;
-          const bool valid = tt < nt && j < lo + p.chunk && j <= pos0 + tt;
+          const bool valid = tt < nt && j < lim && j <= pos0 + tt;
           const uint32_t u = valid ? score_key(s) : 0u;
           scores[tt * p.chunk + (j - lo)] = u;
           if (valid) atomicAdd(&hist[tt * kHistWords + (u >> 22)], 1u << (((u >> 21) & 1u) * 16u));
@@ -528,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- select phase (cluster-uniform control flow)
   if (tid < T) {
     const int tt = tid;
-    const int vis = pos0 + tt + 1;
+    const int vis = max(0, min(pos0 + tt + 1, u_hi) - u_lo);  // visible positions of the unit
     ctl->need_total[tt] = tt < nt ? min(p.K, vis) : 0;
     ctl->radix[tt] = (tt < nt && vis > p.K) ? 1 : 0;
     ctl->need[tt] = ctl->need_total[tt];
@@ -826,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool split = false;
       for (int i = warp * span + lane; i < i_end; i += 32) {
         const uint2 c = G[i];
-        const int r = (int)c.y / p.chunk;
+        const int r = ((int)c.y - u_lo) / chunk;
         const int bk = r == rank ? kMaxCluster + ((int)c.y - lo) / seg : r;
         if (bk != cur) {
           if (cur >= 0) {
@@ -1001,7 +1028,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       eq_before += ctl->weq[tt][w];
     }
     const int my_ties = max(0, min(ctl->weq[tt][warp], ctl->quota[tt] - eq_before));
-    int* out = p.out_idx + (size_t)(t0 + tt) * p.K;
+    const size_t slot_u = ((size_t)(b * p.groups + g) * p.units + unit) * T + tt;
+    int* out = direct ? p.out_idx + (size_t)(t0 + tt) * p.K : p.cand_idx + slot_u * p.K;
+    float* out_sc = direct ? (p.out_score ? p.out_score + (size_t)(t0 + tt) * p.K : nullptr)
+                           : p.cand_score + slot_u * p.K;
     uint32_t* sc = scores + tt * p.chunk;
     int eq_run = 0, sel_run = 0;
     // batches of four 128-key groups: lane holds keys 4*lane..4*lane+3 of each group
@@ -1048,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every lane's keys of the batch are in registers (the scan above), and the staged count
       // never exceeds the keys read so far: the writes land on keys already consumed
       int base = sel_run;
-      if (p.out_score == nullptr) {
+      if (out_sc == nullptr) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
@@ -1064,8 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             if ((take >> (4 * g + k)) & 1u) {
-              if (off + (slot - e_lo) < need_total)
-                p.out_score[(size_t)(t0 + tt) * p.K + off + (slot - e_lo)] = key_score(key[4 * g + k]);
+              if (off + (slot - e_lo) < need_total) out_sc[off + (slot - e_lo)] = key_score(key[4 * g + k]);
               sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
             }
           base += (int)((ttot >> (8 * g)) & 0xffu);
@@ -1083,9 +1112,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rank == 0) {
       for (int r = need_total + tid; r < p.K; r += kThreads) {
         out[r] = -1;
-        if (p.out_score) p.out_score[(size_t)(t0 + tt) * p.K + r] = -INFINITY;
+        if (out_sc) out_sc[r] = -INFINITY;
       }
-      if (tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_total;
+      if (direct && tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_total;
     }
   }
   // peers may still be reading this CTA's counters / candidates
@@ -1097,6 +1126,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
+// Upper bound of the position units per sequence (1: a cluster covers a whole sequence).  Units
+// are used for groups of at most two tokens (decode, speculative pairs) whose sequences may be
+// longer than kUnitSpan, as long as the merge can hold every unit's candidates.
+static int unit_bound(const dsa_li_args& a) {
+  if (a.max_q_per_seq > 2 || a.max_seq_len <= kUnitSpan) return 1;
+  const int u = (a.max_seq_len + kUnitSpan - 1) / kUnitSpan;
+  return (long long)u * a.K <= kMaxUnitCand ? u : 1;
+}
+
+static size_t unit_workspace_bytes(const dsa_li_args& a) {
+  const int ub = unit_bound(a);
+  if (ub <= 1) return 0;
+  const int T = a.max_q_per_seq <= 1 ? 1 : 2;
+  const int groups = (a.max_q_per_seq + T - 1) / T;
+  const size_t slots = (size_t)a.B * groups * ub * T;
+  return (slots * a.K * 4 + 255) / 256 * 256 + (slots * a.K * 4 + 255) / 256 * 256;
+}
+
 template <int D_I, bool FP8, int H_I, int T, bool MX = false>
 static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::string& err) {
   using CF = Cfg<D_I, FP8, H_I, T, MX>;
@@ -1104,6 +1151,10 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   if (!device_info(dev, err)) return DSA_ERR_CUDA;
   const int groups = (a.max_q_per_seq + T - 1) / T;
   const int maxL = std::max(a.max_seq_len, 1);
+  // With units, a cluster is planned for kUnitSpan positions and a sequence takes one cluster
+  // per unit; otherwise for the longest sequence.
+  const int ub = T <= 2 ? unit_bound(a) : 1;
+  const int planL = ub > 1 ? kUnitSpan : maxL;
 
   auto kern = li_topk_kernel<D_I, FP8, H_I, T, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
@@ -1117,8 +1168,8 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   // select phase (which scans each CTA's chunk and does not overlap the stream).
   struct Choice { int ns, c, chunk, smem; };
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int>, Choice> memo;
-  const auto key = std::make_tuple(dev.device, maxL, a.B * groups);
+  static std::map<std::tuple<int, int, int, int>, Choice> memo;
+  const auto key = std::make_tuple(dev.device, maxL, a.B * groups, ub);
   Choice best{0, 0, 0, 0};
   {
     std::lock_guard<std::mutex> lock(mu);
@@ -1127,11 +1178,13 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   }
   if (!best.c) {
     double best_est = 1e300;
-    const long long clusters = (long long)a.B * groups;
     for (int ns = 8; ns >= 2; --ns) {
       for (int c = 1; c <= kMaxCluster; ++c) {
-        const int chunk = ((maxL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
-        if (chunk > 65535 || (long long)chunk * c < maxL) continue;
+        const int chunk = ((planL + c - 1) / c + kTileKeys - 1) / kTileKeys * kTileKeys;
+        if (chunk > 65535 || (long long)chunk * c < planL) continue;
+        if (ub > 1 && chunk * c != kUnitSpan) continue;  // units of exactly kUnitSpan positions
+        const long long units = ub > 1 ? (maxL + (long long)c * chunk - 1) / ((long long)c * chunk) : 1;
+        const long long clusters = (long long)a.B * groups * units;
         const Layout lay(ns, CF::kTileBytes, CF::kQBytes, T, H_I, chunk);
         const int smem = lay.total + 1024;
         if (smem > dev.smem_optin) continue;
@@ -1174,6 +1227,19 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
     memo[key] = best;
   }
   const int best_ns = best.ns, best_c = best.c, best_chunk = best.chunk, best_smem = best.smem;
+  const int units = ub > 1 ? (maxL + best_c * best_chunk - 1) / (best_c * best_chunk) : 1;
+  UnitMergeArgs um{};
+  if (units > 1) {
+    const size_t slots = (size_t)a.B * groups * units * T;
+    const size_t half = (slots * a.K * 4 + 255) / 256 * 256;
+    if (a.workspace == nullptr || a.workspace_bytes < 2 * half) {
+      err = "li_topk: workspace of " + std::to_string(2 * half) + " bytes required (got " +
+            std::to_string(a.workspace_bytes) + ")";
+      return DSA_ERR_INVALID_ARG;
+    }
+    um.cand_idx = reinterpret_cast<int*>(a.workspace);
+    um.cand_score = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.workspace) + half);
+  }
 
   CUtensorMap tm_k, tm_q;
   const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1193,6 +1259,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.groups = groups;
   p.chunk = best_chunk;
   p.C = best_c;
+  p.units = units;
   p.nstage = best_ns;
   p.w = a.w;
   p.q_scale = a.q_scale;
@@ -1206,12 +1273,14 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.q_sf = a.q_sf;
   p.k_sf = a.k_sf;
   p.out_score = a.out_score;
+  p.cand_idx = um.cand_idx;
+  p.cand_score = um.cand_score;
 #ifdef DSA_TEST_HOOKS
   p.stall = g_test_stall;
 #endif
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(best_c * a.B * groups));
+  cfg.gridDim = dim3((unsigned)(best_c * a.B * groups * units));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)best_smem;
   cfg.stream = stream;
@@ -1224,10 +1293,28 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_q, p);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: launch", err);
+  if (units > 1) {
+    um.B = a.B;
+    um.n_q = a.n_q;
+    um.K = a.K;
+    um.T = T;
+    um.groups = groups;
+    um.units = units;
+    um.span = best_c * best_chunk;
+    um.max_pages = a.max_pages;
+    um.seq_lens = a.seq_lens;
+    um.q_start = a.q_start;
+    um.out_idx = a.out_idx;
+    um.out_cnt = a.out_cnt;
+    um.out_score = a.out_score;
+    return launch_unit_merge(um, stream, err);
+  }
   return DSA_OK;
 }
 
 }  // namespace li
+
+size_t li_workspace_bytes(const dsa_li_args& a) { return li::unit_workspace_bytes(a); }
 
 static dsa_status launch_li_topk_T(const dsa_li_args& a, int T, cudaStream_t stream, std::string& err);
 

@@ -84,6 +84,77 @@ __global__ void __launch_bounds__(kThreads)
   if (tid == 0 && a.out_cnt) a.out_cnt[t] = cnt;
 }
 
+// Largest b with q_start[b] <= t.
+DSA_DEV int find_seq(const int* q_start, int B, int t) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (q_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Indexer over position units ("Inference Optimization for Kimi K3.1 Pro", section 5: a local
+// Top-K per range of positions, then a merge of the candidates; here the ranges are units of one
+// sequence on one GPU, so that long and short sequences of one batch spread evenly over the
+// SMs).  One CTA per token whose sequence has more than one unit: the units' candidates (exact
+// top-K of disjoint position ranges with their scores) are merged exactly as above.  Runs as a
+// programmatic dependent of the indexer: nothing is read before that grid has completed.
+__global__ void __launch_bounds__(kThreads)
+    unit_merge_kernel(const UnitMergeArgs a, int ncand_pow2, int k_pow2) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);
+  unsigned long long* sel = key + ncand_pow2;  // (position << 32 | score key) of the selected
+  __shared__ int valid;
+  griddep_wait();
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int b = find_seq(a.q_start, a.B, t);
+  const int qs = a.q_start[b], n_b = a.q_start[b + 1] - qs;
+  const int L = a.seq_lens[b];
+  // the indexer reported (and skipped) a sequence that fails these
+  if (n_b <= 0 || L < n_b || L > a.units * a.span || L > a.max_pages * 64 || qs < 0 ||
+      qs + n_b > a.n_q || n_b > a.groups * a.T || t - qs >= n_b)
+    return;
+  const int n_u = max(1, (L + a.span - 1) / a.span);
+  if (n_u <= 1) return;  // the indexer wrote this token's result
+  const int g = (t - qs) / a.T, tt = (t - qs) % a.T;
+  const int ncand = n_u * a.K;
+  if (tid == 0) valid = 0;
+  for (int i = tid; i < ncand_pow2; i += kThreads) {
+    unsigned long long k = 0ull;  // no candidate: sorts after every real one
+    if (i < ncand) {
+      const int u = i / a.K, r = i % a.K;
+      const size_t at = (((size_t)(b * a.groups + g) * a.units + u) * a.T + tt) * a.K + r;
+      const int j = a.cand_idx[at];
+      // score_key of a finite score is never 0, so real keys stay above "no candidate"
+      if (j >= 0) k = ((unsigned long long)score_key(a.cand_score[at]) << 32) | (0xFFFFFFFFu - (uint32_t)j);
+    }
+    key[i] = k;
+  }
+  __syncthreads();
+  bitonic(key, ncand_pow2, true);
+  int mine = 0;
+  for (int i = tid; i < k_pow2; i += kThreads) {
+    unsigned long long v = ~0ull;  // sorts after every selected position
+    if (i < a.K && key[i] != 0ull) {
+      const uint32_t p = 0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull);
+      v = ((unsigned long long)p << 32) | (key[i] >> 32);
+      ++mine;
+    }
+    sel[i] = v;
+  }
+  atomicAdd(&valid, mine);
+  __syncthreads();
+  bitonic(sel, k_pow2, false);
+  const int cnt = valid;
+  for (int r = tid; r < a.K; r += kThreads) {
+    a.out_idx[(size_t)t * a.K + r] = r < cnt ? (int)(sel[r] >> 32) : -1;
+    if (a.out_score)
+      a.out_score[(size_t)t * a.K + r] = r < cnt ? key_score((uint32_t)(sel[r] & 0xFFFFFFFFull)) : -INFINITY;
+  }
+  if (tid == 0 && a.out_cnt) a.out_cnt[t] = cnt;
+}
+
 }  // namespace merge
 
 dsa_status launch_topk_merge(const dsa_topk_merge_args& a, cudaStream_t stream, std::string& err) {
@@ -98,6 +169,34 @@ dsa_status launch_topk_merge(const dsa_topk_merge_args& a, cudaStream_t stream, 
   topk_merge_kernel<<<a.n_q, kThreads, smem, stream>>>(a, nc, kp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "topk_merge: launch", err);
+  return DSA_OK;
+}
+
+dsa_status launch_unit_merge(const UnitMergeArgs& a, cudaStream_t stream, std::string& err) {
+  using namespace merge;
+  if (a.n_q == 0) return DSA_OK;
+  int nc = 1, kp = 1;
+  while (nc < a.units * a.K) nc <<= 1;
+  while (kp < a.K) kp <<= 1;
+  if (nc > kMaxCand) {
+    err = "li_topk: " + std::to_string(a.units) + " units x K exceed the merge capacity";
+    return DSA_ERR_UNSUPPORTED;
+  }
+  const int smem = nc * 8 + kp * 8;
+  cudaError_t e = cudaFuncSetAttribute(unit_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "li_topk: set unit merge shared memory size", err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_q);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, unit_merge_kernel, a, nc, kp);
+  if (e != cudaSuccess) return cuda_fail(e, "li_topk: unit merge launch", err);
   return DSA_OK;
 }
 

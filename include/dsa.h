@@ -41,7 +41,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 6
+#define DSA_ABI_VERSION 7
 
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -87,6 +87,14 @@ int dsa_abi_version(void);
  * MXFP8_E4M3 with (H_I, d_I) = (64, 128);
  * 1 <= K <= 2048; max_seq_len <= 131072; any number of tokens per sequence (decode, speculative
  * multi-token decode, chunked prefill).
+ *
+ * Position units (decode and two-token groups, max_seq_len > 32768): a sequence longer than one
+ * cluster's span (32768 positions) is split into equal units, each selecting the top-K of its own
+ * positions (with their scores) into `workspace`; a second kernel then merges each such token's
+ * units ("Inference Optimization for Kimi K3.1 Pro", section 5: a local Top-K before the
+ * merge, here over ranges of one sequence on one GPU), so that a batch of short and long
+ * sequences spreads evenly over the SMs.  The result is the same set, in the same order.
+ * dsa_li_workspace_bytes() says how much scratch that takes (0 when no sequence can be split).
  */
 typedef struct {
   int B;            /* sequences                                                         */
@@ -115,7 +123,14 @@ typedef struct {
                              row of scales must be 4-byte aligned (d_I = 128)              */
   float* out_score;       /* [n_q][K] fp32 score of each position in out_idx (-inf for the
                              padding), or NULL: the candidates of a context-parallel shard  */
+  void* workspace;        /* device scratch of dsa_li_workspace_bytes() bytes, 256-B aligned,
+                             or NULL when that is 0; owned by the caller, no initial value */
+  size_t workspace_bytes;
 } dsa_li_args;
+
+/* Scratch that dsa_li_topk needs for these arguments (0 if none).  Host only: reads B, K,
+ * max_seq_len and max_q_per_seq; no CUDA call. */
+size_t dsa_li_workspace_bytes(const dsa_li_args* args);
 
 dsa_status dsa_li_topk(const dsa_li_args* args, dsa_stream_t stream);
 

@@ -29,7 +29,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_abi_version_and_status_strings():
     lib = dsa.load()
-    assert lib.dsa_abi_version() == 6
+    assert lib.dsa_abi_version() == 7
     assert dsa.status_string(0) == "DSA_OK"
     assert dsa.status_string(5) == "DSA_ERR_TIMEOUT"
     assert dsa.status_string(77) == "DSA_ERR_UNKNOWN"
@@ -37,7 +37,7 @@ def test_abi_version_and_status_strings():
 
 def test_struct_layouts_match_header():
     """ctypes mirrors of the argument structs have the C sizes (x86_64 / aarch64 LP64)."""
-    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 14 * 8
+    assert ctypes.sizeof(dsa.LiArgs) == 11 * 4 + 4 + 15 * 8 + 8
     assert ctypes.sizeof(dsa.MergeArgs) == 4 * 4 + 5 * 8
     assert ctypes.sizeof(dsa.SfaArgs) == 12 * 4 + 10 * 8 + 8 + 8
     assert ctypes.sizeof(dsa.PrologArgs) == 10 * 4 + 2 * 4 + 16 * 8 + 8 + 8
@@ -57,6 +57,19 @@ def test_static_scratch_covers_every_automatic_decode_plan():
     q = torch.empty((32, 128, 576), dtype=torch.bfloat16, device="meta")
     idx = torch.empty((32, 2048), dtype=torch.int32, device="meta")
     assert dsa.sfa_workspace_bytes(q, idx, row_splits=32) > dsa.SFA_STATIC_SCRATCH_BYTES
+
+
+def test_li_workspace_bytes_for_position_units():
+    """Scratch for the indexer's position units: none unless a decode or two-token group's
+    sequence can exceed one cluster's span (32768 positions), then one K-row of positions and
+    one of scores per (sequence, unit, token), each array padded to 256 bytes."""
+    assert dsa.li_workspace_bytes(32, 2048, 32768, 1) == 0
+    assert dsa.li_workspace_bytes(1, 2048, 131072, 4096) == 0      # prefill: no units
+    assert dsa.li_workspace_bytes(64, 2048, 131072, 3) == 0        # groups of 4: no units
+    half = lambda n: (n * 4 + 255) // 256 * 256
+    assert dsa.li_workspace_bytes(64, 2048, 131072, 2) == 2 * half(64 * 4 * 2 * 2048)
+    assert dsa.li_workspace_bytes(3, 256, 70000, 1) == 2 * half(3 * 3 * 256)
+    assert dsa.li_workspace_bytes(2, 2048, 32769, 1) == 2 * half(2 * 2 * 2048)
 
 
 def test_page_bytes():

@@ -337,6 +337,47 @@ def test_context_parallel_shards_merge_to_the_full_selection(cuda_lib, name, L, 
         assert np.array_equal(cs[ci >= 0], s_or[ci[ci >= 0]])
 
 
+# ------------------------------------------------------------------ position units
+
+@pytest.mark.parametrize("name,lens,new,exact", [
+    ("decode_int_4k", [40000, 3000, 70000], [1, 2, 1], True),
+    ("decode_32k", [33000, 5000, 65600], [2, 1, 2], False),
+    ("decode_32k_mxfp8", [40000, 900], [1, 1], False),
+    ("decode_32k_fp8", [98400, 32769], [1, 2], False)])
+def test_position_units_long_and_short_sequences(cuda_lib, name, lens, new, exact):
+    """Sequences longer than one cluster's span (32768 positions) are split into units whose
+    local top-K candidates are merged on the GPU; the batch mixes them with short ones.  The
+    selection equals the oracle's over the whole sequence (bit-exact on the integer config,
+    certified near-ties elsewhere), the attention follows, and the scores reported with
+    out_score are the oracle's (exact on the integer config)."""
+    inp_cpu, inp = _small(name, seq_lens=lens, n_new=new)
+    wl = inp_cpu["wl"]
+    assert dsa.li_workspace_bytes(len(lens), wl.K, max(lens), max(new)) > 0
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = list(range(wl.n_q))
+    n_exact, ties = _check_path(inp_cpu, g, toks, exact=exact,
+                                tol=FP8_TOL if wl.li_dtype != "bf16" else BF16_TOL)
+    report({"test": "position_units", "workload": name, "lens": lens, "tokens": len(toks),
+            "exact_rows": n_exact, "near_ties": [[int(t), int(n), round(float(r), 4)]
+                                                 for t, n, r in ties]})
+    # the same selection with scores requested (scores of the merged candidates)
+    score = torch.empty((wl.n_q, wl.K), dtype=torch.float32, device="cuda")
+    idx2, cnt2 = dsa.li_topk(inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"],
+                             inp["q_start"], wl.K, q_scale=inp.get("q_scale"),
+                             k_scale=inp.get("k_scale"), q_sf=inp.get("q_sf"), k_sf=inp.get("k_sf"),
+                             out_score=score, max_seq_len=max(lens), max_q_per_seq=max(new))
+    torch.cuda.synchronize()
+    assert np.array_equal(idx2.cpu().numpy(), g["idx"])
+    sc = score.cpu().numpy()
+    assert np.all(np.isneginf(sc[g["idx"] < 0]))
+    if exact:
+        for t in toks:
+            s_or, _ = oracle.li_scores(inp_cpu, t)
+            row = g["idx"][t]
+            assert np.array_equal(sc[t][row >= 0], s_or[row[row >= 0]])
+
+
 # ------------------------------------------------------------------ FP8 latent cache
 
 @pytest.mark.parametrize("name,lens,new,prefill,K", [
