@@ -51,6 +51,7 @@ constexpr int kCtlBytes = 2560;   // shared control block (mbarriers, counters),
 // of at most one cluster's span; the unit merge sorts units x K candidates in shared memory.
 constexpr int kUnitSpan = 32768;
 constexpr int kMaxUnitCand = 16384;
+constexpr int kMaxUnitSeqs = 256;
 
 struct Params {
   int B, n_q, K, max_pages, num_pages;
@@ -77,6 +78,8 @@ struct Params {
   // these [slots][K] arrays, and the unit merge selects the token's top-K from them
   int* cand_idx;
   float* cand_score;
+  const int* items;     // units > 1: [0] = number of items, [1 + k] = (sequence << 8 | unit) of
+                        // the k-th cluster, written by the unit plan kernel
 #ifdef DSA_TEST_HOOKS
   int stall;            // test build: CTA 0's MMA thread waits on a barrier nothing arrives on
 #endif
@@ -269,13 +272,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = (int)cluster_rank();
-  // Clusters in launch order take the highest units first (only long sequences have them, and
-  // they are full), each sequence's first unit last (short sequences are a single unit): the
-  // longest work starts first.
   const int cl = blockIdx.x / p.C;
-  const int nbg = p.B * p.groups;
-  const int unit = p.units - 1 - cl / nbg;  // position unit of the sequence
-  const int b = cl % nbg / p.groups, g = cl % nbg % p.groups;
+  int b, g, unit;  // sequence, token group, position unit of this cluster
+  if (p.units == 1) {
+    b = cl / p.groups;
+    g = cl % p.groups;
+    unit = 0;
+  } else {
+    // The unit plan kernel ordered the (sequence, unit) items longest first; clusters past the
+    // last item exit at once.  (This launch is its programmatic dependent.)
+    griddep_wait();
+    if (cl >= p.items[0]) return;  // uniform over the cluster
+    const int e = p.items[1 + cl];
+    b = e >> 8;
+    unit = e & 255;
+    g = 0;  // units imply one token group per sequence
+  }
   if (b >= p.B) return;
   const int qs = p.q_start[b];
   const int n_b = p.q_start[b + 1] - qs;
@@ -1124,13 +1136,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();
 }
 
+// Unit plan: one CTA lists the (sequence, unit) items of a launch with position units, in the
+// order of decreasing unit length (ties by sequence), so the longest work starts first; clusters
+// then read their item from the list.  A sequence of L positions has ceil(L / span) units of
+// ceil(L / units) positions.
+__global__ void __launch_bounds__(256) unit_plan_kernel(const int* seq_lens, int B, int span,
+                                                        int* items) {
+  __shared__ int ulen[kMaxUnitSeqs], ucnt[kMaxUnitSeqs];
+  __shared__ int total;
+  const int tid = threadIdx.x;
+  if (tid == 0) total = 0;
+  __syncthreads();
+  if (tid < B) {
+    const int L = max(0, seq_lens[tid]);
+    const int nu = max(1, (L + span - 1) / span);
+    ulen[tid] = (L + nu - 1) / nu;
+    ucnt[tid] = nu;
+    atomicAdd(&total, nu);
+  }
+  __syncthreads();
+  if (tid < B) {
+    int start = 0;
+    for (int j = 0; j < B; ++j)
+      start += (ulen[j] > ulen[tid] || (ulen[j] == ulen[tid] && j < tid)) ? ucnt[j] : 0;
+    for (int u = 0; u < ucnt[tid]; ++u) items[1 + start + u] = (tid << 8) | u;
+  }
+  if (tid == 0) items[0] = total;
+}
+
 // ---------------------------------------------------------------- host side
 
 // Upper bound of the position units per sequence (1: a cluster covers a whole sequence).  Units
 // are used for groups of at most two tokens (decode, speculative pairs) whose sequences may be
 // longer than kUnitSpan, as long as the merge can hold every unit's candidates.
 static int unit_bound(const dsa_li_args& a) {
-  if (a.max_q_per_seq > 2 || a.max_seq_len <= kUnitSpan) return 1;
+  // (the longest-first order of the units is derived in every CTA: at most kMaxUnitSeqs)
+  if (a.max_q_per_seq > 2 || a.max_seq_len <= kUnitSpan || a.B > kMaxUnitSeqs) return 1;
   const int u = (a.max_seq_len + kUnitSpan - 1) / kUnitSpan;
   return (long long)u * a.K <= kMaxUnitCand ? u : 1;
 }
@@ -1141,7 +1182,7 @@ static size_t unit_workspace_bytes(const dsa_li_args& a) {
   const int T = a.max_q_per_seq <= 1 ? 1 : 2;
   const int groups = (a.max_q_per_seq + T - 1) / T;
   const size_t slots = (size_t)a.B * groups * ub * T;
-  return (slots * a.K * 4 + 255) / 256 * 256 + (slots * a.K * 4 + 255) / 256 * 256;
+  return 2 * ((slots * a.K * 4 + 255) / 256 * 256) + ((1 + (size_t)a.B * ub) * 4 + 255) / 256 * 256;
 }
 
 template <int D_I, bool FP8, int H_I, int T, bool MX = false>
@@ -1229,16 +1270,22 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   const int best_ns = best.ns, best_c = best.c, best_chunk = best.chunk, best_smem = best.smem;
   const int units = ub > 1 ? (maxL + best_c * best_chunk - 1) / (best_c * best_chunk) : 1;
   UnitMergeArgs um{};
+  int* items = nullptr;
   if (units > 1) {
     const size_t slots = (size_t)a.B * groups * units * T;
     const size_t half = (slots * a.K * 4 + 255) / 256 * 256;
-    if (a.workspace == nullptr || a.workspace_bytes < 2 * half) {
-      err = "li_topk: workspace of " + std::to_string(2 * half) + " bytes required (got " +
+    const size_t need = 2 * half + ((1 + (size_t)a.B * units) * 4 + 255) / 256 * 256;
+    if (a.workspace == nullptr || a.workspace_bytes < need) {
+      err = "li_topk: workspace of " + std::to_string(need) + " bytes required (got " +
             std::to_string(a.workspace_bytes) + ")";
       return DSA_ERR_INVALID_ARG;
     }
     um.cand_idx = reinterpret_cast<int*>(a.workspace);
     um.cand_score = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.workspace) + half);
+    items = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(a.workspace) + 2 * half);
+    unit_plan_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.B, best_c * best_chunk, items);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "li_topk: unit plan launch", err);
   }
 
   CUtensorMap tm_k, tm_q;
@@ -1275,6 +1322,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   p.out_score = a.out_score;
   p.cand_idx = um.cand_idx;
   p.cand_score = um.cand_score;
+  p.items = items;
 #ifdef DSA_TEST_HOOKS
   p.stall = g_test_stall;
 #endif
@@ -1284,13 +1332,16 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)best_smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)best_c;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // with units: a programmatic dependent of the unit plan (waits for it before any read)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = units > 1 ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_q, p);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: launch", err);
   if (units > 1) {

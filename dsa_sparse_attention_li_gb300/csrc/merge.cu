@@ -94,18 +94,50 @@ DSA_DEV int find_seq(const int* q_start, int B, int t) {
   return lo;
 }
 
+// Exclusive prefix sum over the 1024 threads of the block (wsum: 32 words of shared memory).
+DSA_DEV uint32_t block_excl_scan(uint32_t v, uint32_t* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = wsum[lane];
+    uint32_t z = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    wsum[lane] = z - w;
+  }
+  __syncthreads();
+  const uint32_t r = wsum[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
 // Indexer over position units ("Inference Optimization for Kimi K3.1 Pro", section 5: a local
 // Top-K per range of positions, then a merge of the candidates; here the ranges are units of one
 // sequence on one GPU, so that long and short sequences of one batch spread evenly over the
-// SMs).  One CTA per token whose sequence has more than one unit: the units' candidates (exact
-// top-K of disjoint position ranges with their scores) are merged exactly as above.  Runs as a
-// programmatic dependent of the indexer: nothing is read before that grid has completed.
+// SMs).  One CTA per token whose sequence has more than one unit.  Its units' candidates (the
+// exact top-K of disjoint, ascending position ranges, each list ascending with -1 padding) are
+// concatenated in unit order, which keeps the positions ascending; a radix select over the
+// order-preserving score keys (11, 11 and 10 bits) finds the K-th largest key and how many keys
+// equal to it are taken, the lowest positions first; one ordered compaction writes the result.
+// Runs as a programmatic dependent of the indexer: nothing is read before that grid completed.
 __global__ void __launch_bounds__(kThreads)
-    unit_merge_kernel(const UnitMergeArgs a, int ncand_pow2, int k_pow2) {
+    unit_merge_kernel(const UnitMergeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem_raw);
-  unsigned long long* sel = key + ncand_pow2;  // (position << 32 | score key) of the selected
-  __shared__ int valid;
+  __shared__ uint32_t hist[2048];
+  __shared__ uint32_t wsum[32];
+  __shared__ uint32_t found[2];
+  uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);   // [units * K] score keys, 0 = none
+  int* pos = reinterpret_cast<int*>(key + a.units * a.K);  // [units * K]
   griddep_wait();
   const int t = blockIdx.x, tid = threadIdx.x;
   const int b = find_seq(a.q_start, a.B, t);
@@ -119,40 +151,92 @@ __global__ void __launch_bounds__(kThreads)
   if (n_u <= 1) return;  // the indexer wrote this token's result
   const int g = (t - qs) / a.T, tt = (t - qs) % a.T;
   const int ncand = n_u * a.K;
-  if (tid == 0) valid = 0;
-  for (int i = tid; i < ncand_pow2; i += kThreads) {
-    unsigned long long k = 0ull;  // no candidate: sorts after every real one
-    if (i < ncand) {
-      const int u = i / a.K, r = i % a.K;
-      const size_t at = (((size_t)(b * a.groups + g) * a.units + u) * a.T + tt) * a.K + r;
-      const int j = a.cand_idx[at];
-      // score_key of a finite score is never 0, so real keys stay above "no candidate"
-      if (j >= 0) k = ((unsigned long long)score_key(a.cand_score[at]) << 32) | (0xFFFFFFFFu - (uint32_t)j);
-    }
-    key[i] = k;
+  uint32_t nvalid = 0;
+  for (int i = tid; i < ncand; i += kThreads) {
+    const int u = i / a.K, r = i % a.K;
+    const size_t at = (((size_t)(b * a.groups + g) * a.units + u) * a.T + tt) * a.K + r;
+    const int j = a.cand_idx[at];
+    // score_key of a finite score is never 0
+    key[i] = j >= 0 ? score_key(a.cand_score[at]) : 0u;
+    pos[i] = j;
+    nvalid += j >= 0;
   }
+  const uint32_t total = block_excl_scan(nvalid, wsum) + nvalid;  // the last thread's is the sum
+  if (tid == kThreads - 1) found[0] = total;
   __syncthreads();
-  bitonic(key, ncand_pow2, true);
-  int mine = 0;
-  for (int i = tid; i < k_pow2; i += kThreads) {
-    unsigned long long v = ~0ull;  // sorts after every selected position
-    if (i < a.K && key[i] != 0ull) {
-      const uint32_t p = 0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull);
-      v = ((unsigned long long)p << 32) | (key[i] >> 32);
-      ++mine;
+  const uint32_t all = found[0];
+  const uint32_t cnt = min(all, (uint32_t)a.K);
+  uint32_t thr = 0u, need_eq = 0u;  // take keys > thr, and the first need_eq keys == thr
+  if (all > (uint32_t)a.K) {
+    uint32_t prefix = 0u, pmask = 0u, need = (uint32_t)a.K;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const int nbins = pass == 2 ? 1024 : 2048;
+      const uint32_t bmask = (uint32_t)nbins - 1u;
+      for (int i = tid; i < 2048; i += kThreads) hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < ncand; i += kThreads) {
+        const uint32_t k = key[i];
+        if (k != 0u && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & bmask], 1u);
+      }
+      __syncthreads();
+      // thread i owns bins 2p + 1 and 2p with p = 1023 - i: the exclusive prefix sum counts the
+      // keys in higher bins
+      const int pr = 1023 - tid;
+      const uint32_t c_hi = hist[2 * pr + 1], c_lo = hist[2 * pr];
+      const uint32_t above = block_excl_scan(c_hi + c_lo, wsum);
+      if (above < need && above + c_hi >= need) {
+        found[0] = (uint32_t)(2 * pr + 1);
+        found[1] = need - above;
+      } else if (above + c_hi < need && above + c_hi + c_lo >= need) {
+        found[0] = (uint32_t)(2 * pr);
+        found[1] = need - above - c_hi;
+      }
+      __syncthreads();
+      prefix |= found[0] << shift;
+      need = found[1];
+      pmask |= bmask << shift;
+      __syncthreads();
     }
-    sel[i] = v;
+    thr = prefix;
+    need_eq = need;
   }
-  atomicAdd(&valid, mine);
-  __syncthreads();
-  bitonic(sel, k_pow2, false);
-  const int cnt = valid;
-  for (int r = tid; r < a.K; r += kThreads) {
-    a.out_idx[(size_t)t * a.K + r] = r < cnt ? (int)(sel[r] >> 32) : -1;
-    if (a.out_score)
-      a.out_score[(size_t)t * a.K + r] = r < cnt ? key_score((uint32_t)(sel[r] & 0xFFFFFFFFull)) : -INFINITY;
+  // ordered compaction: thread i takes the contiguous run [i * per, (i + 1) * per)
+  const int per = (ncand + kThreads - 1) / kThreads;
+  const int c0 = min(ncand, tid * per), c1 = min(ncand, c0 + per);
+  uint32_t eq = 0;
+  for (int i = c0; i < c1; ++i) eq += (key[i] == thr && thr != 0u);
+  uint32_t eq_before = block_excl_scan(eq, wsum);
+  uint32_t take = 0;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = key[i];
+    if (k > thr) {
+      ++take;
+    } else if (k == thr && thr != 0u) {
+      if (eq_before < need_eq) ++take;
+      ++eq_before;
+    }
   }
-  if (tid == 0 && a.out_cnt) a.out_cnt[t] = cnt;
+  uint32_t at = block_excl_scan(take, wsum);
+  eq_before -= eq;  // back to this run's first tie
+  int* out = a.out_idx + (size_t)t * a.K;
+  float* osc = a.out_score ? a.out_score + (size_t)t * a.K : nullptr;
+  for (int i = c0; i < c1; ++i) {
+    const uint32_t k = key[i];
+    bool sel = k > thr;
+    if (k == thr && thr != 0u) sel = eq_before++ < need_eq;
+    if (sel) {
+      out[at] = pos[i];
+      if (osc) osc[at] = key_score(k);
+      ++at;
+    }
+  }
+  for (int r = (int)cnt + tid; r < a.K; r += kThreads) {
+    out[r] = -1;
+    if (osc) osc[r] = -INFINITY;
+  }
+  if (tid == 0 && a.out_cnt) a.out_cnt[t] = (int)cnt;
 }
 
 }  // namespace merge
@@ -175,14 +259,11 @@ dsa_status launch_topk_merge(const dsa_topk_merge_args& a, cudaStream_t stream, 
 dsa_status launch_unit_merge(const UnitMergeArgs& a, cudaStream_t stream, std::string& err) {
   using namespace merge;
   if (a.n_q == 0) return DSA_OK;
-  int nc = 1, kp = 1;
-  while (nc < a.units * a.K) nc <<= 1;
-  while (kp < a.K) kp <<= 1;
-  if (nc > kMaxCand) {
+  if ((long long)a.units * a.K > kMaxCand) {
     err = "li_topk: " + std::to_string(a.units) + " units x K exceed the merge capacity";
     return DSA_ERR_UNSUPPORTED;
   }
-  const int smem = nc * 8 + kp * 8;
+  const int smem = a.units * a.K * 8;
   cudaError_t e = cudaFuncSetAttribute(unit_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: set unit merge shared memory size", err);
   cudaLaunchConfig_t cfg = {};
@@ -195,7 +276,7 @@ dsa_status launch_unit_merge(const UnitMergeArgs& a, cudaStream_t stream, std::s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, unit_merge_kernel, a, nc, kp);
+  e = cudaLaunchKernelEx(&cfg, unit_merge_kernel, a);
   if (e != cudaSuccess) return cuda_fail(e, "li_topk: unit merge launch", err);
   return DSA_OK;
 }

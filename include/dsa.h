@@ -88,7 +88,7 @@ int dsa_abi_version(void);
  * 1 <= K <= 2048; max_seq_len <= 131072; any number of tokens per sequence (decode, speculative
  * multi-token decode, chunked prefill).
  *
- * Position units (decode and two-token groups, max_seq_len > 32768): a sequence longer than one
+ * Position units (decode and two-token groups, max_seq_len > 32768, B <= 256): a sequence longer than one
  * cluster's span (32768 positions) is split into equal units, each selecting the top-K of its own
  * positions (with their scores) into `workspace`; a second kernel then merges each such token's
  * units ("Inference Optimization for Kimi K3.1 Pro", section 5: a local Top-K before the

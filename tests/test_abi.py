@@ -61,15 +61,18 @@ def test_static_scratch_covers_every_automatic_decode_plan():
 
 def test_li_workspace_bytes_for_position_units():
     """Scratch for the indexer's position units: none unless a decode or two-token group's
-    sequence can exceed one cluster's span (32768 positions), then one K-row of positions and
-    one of scores per (sequence, unit, token), each array padded to 256 bytes."""
+    sequence can exceed one cluster's span (32768 positions) and the batch has at most 256
+    sequences, then one K-row of positions and one of scores per (sequence, unit, token) and
+    the unit plan's item list, each array padded to 256 bytes."""
     assert dsa.li_workspace_bytes(32, 2048, 32768, 1) == 0
     assert dsa.li_workspace_bytes(1, 2048, 131072, 4096) == 0      # prefill: no units
     assert dsa.li_workspace_bytes(64, 2048, 131072, 3) == 0        # groups of 4: no units
     half = lambda n: (n * 4 + 255) // 256 * 256
-    assert dsa.li_workspace_bytes(64, 2048, 131072, 2) == 2 * half(64 * 4 * 2 * 2048)
-    assert dsa.li_workspace_bytes(3, 256, 70000, 1) == 2 * half(3 * 3 * 256)
-    assert dsa.li_workspace_bytes(2, 2048, 32769, 1) == 2 * half(2 * 2 * 2048)
+    # + the item list of the unit plan: a count and one word per (sequence, unit)
+    assert dsa.li_workspace_bytes(64, 2048, 131072, 2) == 2 * half(64 * 4 * 2 * 2048) + half(1 + 64 * 4)
+    assert dsa.li_workspace_bytes(3, 256, 70000, 1) == 2 * half(3 * 3 * 256) + half(1 + 3 * 3)
+    assert dsa.li_workspace_bytes(2, 2048, 32769, 1) == 2 * half(2 * 2 * 2048) + half(1 + 2 * 2)
+    assert dsa.li_workspace_bytes(257, 2048, 65536, 1) == 0  # more sequences than the plan orders
 
 
 def test_page_bytes():
