@@ -135,6 +135,7 @@ struct Ctl {
   uint64_t qbar;
   uint64_t drain;
   uint64_t sinit;  // MXFP8: the first scale cells are in tensor memory
+  uint64_t cand_bar;  // candidate path: the other ranks' candidate keys and sure counts are here
 #ifdef DSA_TEST_HOOKS
   uint64_t never;  // test build: no thread ever arrives here
 #endif
@@ -149,6 +150,7 @@ struct Ctl {
   int offset[4], quota[4];
   int found_bin[4], found_need[4];
   int wgt[4][kThreads / 32], weq[4][kThreads / 32];  // per-warp counts above / at the threshold
+  int wcnd[4][kThreads / 32];  // candidate path: per-warp candidates in the threshold bin
   // candidate path of the select (see the select phase)
   int cand_total[4];          // keys of the whole cluster in the threshold bin of the first pass
   int few_cnt;                // candidates sharing the 22-bit prefix (local resolution)
@@ -334,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->qbar, 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->sinit, 256);  // both epilogue groups
+    mbar_init(&ctl->cand_bar, 1);
 #ifdef DSA_TEST_HOOKS
     mbar_init(&ctl->never, 1);
 #endif
@@ -632,16 +635,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (fast) {
-    // ---- candidate path: 2 cluster barriers instead of 4.
-    // (a) per warp segment: keys certainly selected ("sure": above the threshold bin, or every
-    //     visible key of a token that sees fewer than K positions) are counted, keys in the
-    //     threshold bin are written, in ascending position order, to this CTA's candidate list
-    //     in the first half of the (now idle) TMA ring.
+    // ---- candidate path: one cluster barrier.  Every CTA reads how many keys each rank holds in
+    // the threshold bin, so the cluster's candidate list has a known layout (rank order, then
+    // position order) and every CTA pushes its candidates' keys straight into every other CTA's
+    // copy of the list (asynchronous stores counted on the receiver's mbarrier); each CTA then
+    // resolves the threshold and the per-rank counts from its full copy.
     const int cap = p.nstage * CF::kTileBytes / 2 / 8 / T;
-    uint2* own_list = reinterpret_cast<uint2*>(stage_base);
-    uint2* gath = reinterpret_cast<uint2*>(stage_base + p.nstage * CF::kTileBytes / 2);
-    // a1: one pass over the warp's segment: sure keys counted, candidates marked (bit 4*step + k
-    // of the lane's word) and counted per lane; then a warp scan of the lane counts
+    uint32_t* gk = reinterpret_cast<uint32_t*>(stage_base);  // [T][cap] the cluster's candidates
+    // (a) candidates per rank in the threshold bin (first-pass histograms), list offsets, and the
+    //     bytes the other ranks will store here: their candidates and their sure counts
+    if (tid < T * p.C) {
+      const int tt = tid / p.C, r = tid % p.C;
+      int n = 0;
+      if (ctl->radix[tt]) {
+        const uint32_t bin = ctl->prefix[tt] >> 21;
+        const uint32_t w = ld_cluster_u32(map_cluster(hist + tt * kHistWords + (bin >> 1), (uint32_t)r));
+        n = (int)((w >> (16u * (bin & 1u))) & 0xffffu);
+      }
+      ctl->rn[tt][r] = n;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t bytes = 4u * T * (uint32_t)(p.C - 1);
+      for (int tt = 0; tt < T; ++tt) {
+        int o = 0;
+        for (int r = 0; r < p.C; ++r) {
+          ctl->roff[tt][r] = o;
+          o += ctl->rn[tt][r];
+          if (r != rank) bytes += 4u * (uint32_t)ctl->rn[tt][r];
+        }
+        ctl->cand_total[tt] = o;  // equals the histogram's count of the bin
+      }
+      // (a phase may count stored bytes before this arrival sets how many to expect)
+      mbar_arrive_expect_tx(&ctl->cand_bar, bytes);
+    }
+    // (b) per warp segment: keys certainly selected ("sure": above the threshold bin, or every
+    //     visible key of a token that sees fewer than K positions) are counted, keys in the
+    //     threshold bin marked (bit 4*step + k of the lane's word) and counted per lane
     uint64_t cbits[4];
     int lane_base[4];
 #pragma unroll
@@ -674,81 +704,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t cand = __shfl_sync(0xffffffffu, inc, 31);
       if (lane == 0) {
         ctl->wgt[tt][warp] = (int)sure;
-        ctl->weq[tt][warp] = (int)cand;  // candidates of the warp (replaced in step d)
+        ctl->wcnd[tt][warp] = (int)cand;
       }
     }
     __syncthreads();
-    // a2: each lane writes its candidates (lane-major within the warp; a warp's candidates stay
-    // contiguous and in warp order, which is all the per-warp counting below needs)
+    // (c) each lane stores its candidates' keys at their place in the cluster's list (this rank's
+    //     range, warps in order, lane-major within a warp) here and in every other CTA, and the
+    //     CTA's sure counts go to every other CTA
+    if (tid < T) {
+      int g = 0;
+      for (int w = 0; w < kThreads / 32; ++w) g += ctl->wgt[tid][w];
+      ctl->rsure[tid][rank] = g;
+      for (int r = 0; r < p.C; ++r)
+        if (r != rank)
+          st_async_b32(map_cluster(&ctl->rsure[tid][rank], (uint32_t)r), (uint32_t)g,
+                       map_cluster(&ctl->cand_bar, (uint32_t)r));
+    }
 #pragma unroll
     for (int tt = 0; tt < T; ++tt) {
       if (!ctl->radix[tt]) continue;
       const uint32_t* sc = scores + tt * p.chunk;
-      int slot = lane_base[tt];
-      for (int w = 0; w < warp; ++w) slot += ctl->weq[tt][w];
-      uint2* dst = own_list + tt * cap;
+      int slot = ctl->roff[tt][rank] + lane_base[tt];
+      for (int w = 0; w < warp; ++w) slot += ctl->wcnd[tt][w];
       uint64_t bits = cbits[tt];
       while (bits) {
         const int bit = __ffsll((long long)bits) - 1;
         bits &= bits - 1ull;
-        const int e = e_lo + 128 * (bit >> 2) + 4 * lane + (bit & 3);
-        dst[slot++] = make_uint2(sc[e], (uint32_t)(lo + e));
+        const uint32_t key = sc[e_lo + 128 * (bit >> 2) + 4 * lane + (bit & 3)];
+        gk[tt * cap + slot] = key;
+        for (int r = 0; r < p.C; ++r)
+          if (r != rank)
+            st_async_b32(map_cluster(gk + tt * cap + slot, (uint32_t)r), key,
+                         map_cluster(&ctl->cand_bar, (uint32_t)r));
+        ++slot;
       }
     }
-    __syncthreads();
-    if (tid < T) {
-      int g = 0, c = 0;
-      for (int w = 0; w < kThreads / 32; ++w) {
-        g += ctl->wgt[tid][w];
-        c += ctl->weq[tid][w];
-      }
-      ctl->cnt_gt[tid] = g;  // this CTA's sure keys (read by the cluster)
-      ctl->own_cnt[tid] = c;
+    cluster_arrive();  // this CTA has finished reading and storing into the other CTAs' memory
+    {
+      const bool ok = mbar_wait<true>(&ctl->cand_bar, 0u, abort, p.status);
+      (void)ok;  // after a timeout the candidates are incomplete: the result is unspecified
     }
-    cluster_sync();
-    // (b) read every rank's sure count and gather every rank's candidates (rank order)
-    if (tid < T * p.C) {
-      const int tt = tid / p.C, r = tid % p.C;
-      ctl->rsure[tt][r] = (int)ld_cluster_u32(map_cluster(&ctl->cnt_gt[tt], (uint32_t)r));
-      ctl->rn[tt][r] = ctl->radix[tt] ? (int)ld_cluster_u32(map_cluster(&ctl->own_cnt[tt], (uint32_t)r)) : 0;
-    }
-    __syncthreads();
-    if (tid < T) {
-      int o = 0;
-      for (int r = 0; r < p.C; ++r) {
-        ctl->roff[tid][r] = o;
-        o += ctl->rn[tid][r];
-      }
-      ctl->cand_total[tid] = o;  // equals the histogram count unless a score was NaN
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int tt = 0; tt < T; ++tt) {
-      if (!ctl->radix[tt]) continue;
-      const int n = ctl->cand_total[tt];
-      // four loads in flight per thread before their stores
-#pragma unroll 1
-      for (int i0 = tid; i0 < n; i0 += 4 * kThreads) {
-        uint2 v[4];
-        int at[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * kThreads;
-          at[u] = i;
-          if (i < n) {
-            int r = 0;
-            while (r + 1 < p.C && ctl->roff[tt][r + 1] <= i) ++r;
-            v[u] = ld_cluster_v2(map_cluster(own_list + tt * cap + (i - ctl->roff[tt][r]), (uint32_t)r));
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (at[u] < n) gath[tt * cap + at[u]] = v[u];
-      }
-    }
-    cluster_arrive();  // this CTA has finished reading the other CTAs' shared memory
-    __syncthreads();
-    // (c) the remaining 21 bits among the gathered candidates, locally (no cluster barrier):
+    __syncthreads();  // every thread's own stores into gk are visible too
+    // (d) the remaining 21 bits among the gathered candidates, locally (no cluster barrier;
+    //     every peer has finished reading this CTA's histogram before sending its candidates):
     // a histogram of bits 20..10, then the last 10 bits directly among the few candidates that
     // share the 22-bit prefix (a histogram again when there are more than kFew)
     constexpr int kFew = 64;
@@ -757,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tt = 0; tt < T; ++tt) {
       if (!ctl->radix[tt]) continue;
       const int n = ctl->cand_total[tt];
-      const uint2* G = gath + tt * cap;
+      const uint32_t* G = gk + tt * cap;
       uint32_t* h = hist;
       {  // bits 20..10
         const uint32_t pref = ctl->prefix[tt];
@@ -765,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) ctl->few_cnt = 0;
         __syncthreads();
         for (int i = tid; i < n; i += kThreads) {
-          const uint32_t u = G[i].x;
+          const uint32_t u = G[i];
           if ((u & 0xffe00000u) == pref) {
             const uint32_t bin = (u >> 10) & 2047u;
             atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
@@ -781,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t pref = ctl->prefix[tt];
       for (int i = tid; i < n; i += kThreads) {
-        const uint32_t u = G[i].x;
+        const uint32_t u = G[i];
         if ((u & 0xfffffc00u) == pref) {
           const int slot = atomicAdd(&ctl->few_cnt, 1);
           if (slot < kFew) few[slot] = u;
@@ -814,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = tid; i < kHistWords; i += kThreads) h[i] = 0u;
         __syncthreads();
         for (int i = tid; i < n; i += kThreads) {
-          const uint32_t u = G[i].x;
+          const uint32_t u = G[i];
           if ((u & 0xfffffc00u) == pref) {
             const uint32_t bin = u & 1023u;
             atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) * 16u));
@@ -829,64 +827,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
       }
     }
-    // (d) candidates above / at the threshold per rank, and per warp of this CTA.  The gathered
-    //     list is in (rank, position) order, so runs of equal owners aggregate within a warp.
+    // (e) candidates above / at the threshold per rank (its range of the list), and per warp of
+    //     this CTA (its range within this rank's)
     if (tid < T * p.C) {
       ctl->rgt[tid / p.C][tid % p.C] = 0;
       ctl->req[tid / p.C][tid % p.C] = 0;
     }
-    if (tid < T * (kThreads / 32)) {
-      const int tt = tid / (kThreads / 32), w = tid % (kThreads / 32);
-      if (ctl->radix[tt]) ctl->weq[tt][w] = 0;
-    }
     __syncthreads();
 #pragma unroll 1
     for (int tt = 0; tt < T; ++tt) {
-      if (!ctl->radix[tt]) continue;
-      const int n = ctl->cand_total[tt];
-      const uint2* G = gath + tt * cap;
+      if (!ctl->radix[tt]) continue;  // uniform over the block
       const uint32_t thr = ctl->prefix[tt];
-      // Owner bucket of a candidate: its rank, or kMaxCluster + warp for this CTA's own keys.
-      // Buckets are contiguous runs of the list; a lane walks its share in index order and
-      // flushes its counts when the bucket changes.
-      auto flush = [&](int bk, int ng, int ne) {
-        if (bk < 0 || (ng == 0 && ne == 0)) return;
-        const int r = bk < kMaxCluster ? bk : rank;
-        if (ng) atomicAdd(&ctl->rgt[tt][r], ng);
-        if (ne) atomicAdd(&ctl->req[tt][r], ne);
-        if (bk >= kMaxCluster) {
-          if (ng) atomicAdd(&ctl->wgt[tt][bk - kMaxCluster], ng);
-          if (ne) atomicAdd(&ctl->weq[tt][bk - kMaxCluster], ne);
+      const uint32_t* G = gk + tt * cap;
+      for (int r = warp; r < p.C; r += kThreads / 32) {
+        const int r0 = ctl->roff[tt][r], r1 = r0 + ctl->rn[tt][r];
+        uint32_t ng = 0, ne = 0;
+        for (int i = r0 + lane; i < r1; i += 32) {
+          ng += G[i] > thr;
+          ne += G[i] == thr;
         }
-      };
-      const int span = ((n + kThreads / 32 - 1) / (kThreads / 32) + 31) / 32 * 32;
-      const int i_end = min(n, warp * span + span);
-      int cur = -1, ng = 0, ne = 0;
-      bool split = false;
-      for (int i = warp * span + lane; i < i_end; i += 32) {
-        const uint2 c = G[i];
-        const int r = ((int)c.y - u_lo) / chunk;
-        const int bk = r == rank ? kMaxCluster + ((int)c.y - lo) / seg : r;
-        if (bk != cur) {
-          if (cur >= 0) {
-            flush(cur, ng, ne);
-            split = true;
-          }
-          cur = bk;
-          ng = ne = 0;
+        ng = __reduce_add_sync(0xffffffffu, ng);
+        ne = __reduce_add_sync(0xffffffffu, ne);
+        if (lane == 0) {
+          ctl->rgt[tt][r] = (int)ng;
+          ctl->req[tt][r] = (int)ne;
         }
-        ng += c.x > thr;
-        ne += c.x == thr;
       }
-      // usual case: the whole warp saw one bucket -> one reduction and one atomic per counter
-      const int lead = __shfl_sync(0xffffffffu, cur, 0);
-      if (__all_sync(0xffffffffu, !split && (cur == lead || cur < 0))) {
-        const int sg = (int)__reduce_add_sync(0xffffffffu, (uint32_t)ng);
-        const int se = (int)__reduce_add_sync(0xffffffffu, (uint32_t)ne);
-        if (lane == 0) flush(lead, sg, se);
-      } else {
-        flush(cur, ng, ne);
+      {
+        int w0 = ctl->roff[tt][rank];
+        for (int w = 0; w < warp; ++w) w0 += ctl->wcnd[tt][w];
+        const int w1 = w0 + ctl->wcnd[tt][warp];
+        uint32_t ng = 0, ne = 0;
+        for (int i = w0 + lane; i < w1; i += 32) {
+          ng += G[i] > thr;
+          ne += G[i] == thr;
+        }
+        ng = __reduce_add_sync(0xffffffffu, ng);
+        ne = __reduce_add_sync(0xffffffffu, ne);
+        if (lane == 0) {
+          ctl->wgt[tt][warp] += (int)ng;  // sure keys + candidates above the threshold
+          ctl->weq[tt][warp] = (int)ne;
+        }
       }
+    }
+    if (tid < T * (kThreads / 32)) {
+      const int tt = tid / (kThreads / 32), w = tid % (kThreads / 32);
+      if (!ctl->radix[tt]) ctl->weq[tt][w] = 0;
     }
     __syncthreads();
     if (tid < T) {
