@@ -176,9 +176,15 @@ __global__ void __launch_bounds__(kThreads)
       const uint32_t bmask = (uint32_t)nbins - 1u;
       for (int i = tid; i < 2048; i += kThreads) hist[i] = 0u;
       __syncthreads();
-      for (int i = tid; i < ncand; i += kThreads) {
-        const uint32_t k = key[i];
-        if (k != 0u && (k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & bmask], 1u);
+      // The candidates are the units' top scores: most share a few high bins, so the lanes of a
+      // warp that hit the same bin add their count with one atomic.
+      for (int i0 = 0; i0 < ncand; i0 += kThreads) {
+        const int i = i0 + tid;
+        const uint32_t k = i < ncand ? key[i] : 0u;
+        const bool hit = k != 0u && (k & pmask) == prefix;
+        const uint32_t bin = hit ? (k >> shift) & bmask : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (hit && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
       }
       __syncthreads();
       // thread i owns bins 2p + 1 and 2p with p = 1023 - i: the exclusive prefix sum counts the
