@@ -1129,25 +1129,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) unit_plan_kernel(const int* seq_lens, int B, int span,
                                                         int* items) {
   __shared__ int ulen[kMaxUnitSeqs], ucnt[kMaxUnitSeqs];
-  __shared__ int total;
-  const int tid = threadIdx.x;
-  if (tid == 0) total = 0;
-  __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < B) {
     const int L = max(0, seq_lens[tid]);
     const int nu = max(1, (L + span - 1) / span);
     ulen[tid] = (L + nu - 1) / nu;
     ucnt[tid] = nu;
-    atomicAdd(&total, nu);
   }
   __syncthreads();
-  if (tid < B) {
+  // a warp per sequence: its lanes count the units of the sequences ordered before it
+  for (int i = warp; i < B; i += 8) {
+    const int li = ulen[i];
     int start = 0;
-    for (int j = 0; j < B; ++j)
-      start += (ulen[j] > ulen[tid] || (ulen[j] == ulen[tid] && j < tid)) ? ucnt[j] : 0;
-    for (int u = 0; u < ucnt[tid]; ++u) items[1 + start + u] = (tid << 8) | u;
+    for (int j = lane; j < B; j += 32)
+      start += (ulen[j] > li || (ulen[j] == li && j < i)) ? ucnt[j] : 0;
+    start = (int)__reduce_add_sync(0xffffffffu, (uint32_t)start);
+    if (lane < ucnt[i]) items[1 + start + lane] = (i << 8) | lane;
   }
-  if (tid == 0) items[0] = total;
+  if (warp == 0) {
+    int total = 0;
+    for (int j = lane; j < B; j += 32) total += ucnt[j];
+    total = (int)__reduce_add_sync(0xffffffffu, (uint32_t)total);
+    if (lane == 0) items[0] = total;
+  }
 }
 
 // ---------------------------------------------------------------- host side

@@ -151,15 +151,34 @@ __global__ void __launch_bounds__(kThreads)
   if (n_u <= 1) return;  // the indexer wrote this token's result
   const int g = (t - qs) / a.T, tt = (t - qs) % a.T;
   const int ncand = n_u * a.K;
+  // every load of a thread in flight at once: units x ceil(K / threads) <= 16 pairs
   uint32_t nvalid = 0;
-  for (int i = tid; i < ncand; i += kThreads) {
-    const int u = i / a.K, r = i % a.K;
-    const size_t at = (((size_t)(b * a.groups + g) * a.units + u) * a.T + tt) * a.K + r;
-    const int j = a.cand_idx[at];
-    // score_key of a finite score is never 0
-    key[i] = j >= 0 ? score_key(a.cand_score[at]) : 0u;
-    pos[i] = j;
-    nvalid += j >= 0;
+  {
+    constexpr int kPer = kMaxCand / kThreads;
+    int jv[kPer];
+    float sv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * kThreads;
+      jv[k] = -1;
+      sv[k] = 0.f;
+      if (i < ncand) {
+        const int u = i / a.K, r = i - u * a.K;
+        const size_t at = (((size_t)(b * a.groups + g) * a.units + u) * a.T + tt) * a.K + r;
+        jv[k] = __ldcg(a.cand_idx + at);
+        sv[k] = __ldcg(a.cand_score + at);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * kThreads;
+      if (i < ncand) {
+        // score_key of a finite score is never 0
+        key[i] = jv[k] >= 0 ? score_key(sv[k]) : 0u;
+        pos[i] = jv[k];
+        nvalid += jv[k] >= 0;
+      }
+    }
   }
   const uint32_t total = block_excl_scan(nvalid, wsum) + nvalid;  // the last thread's is the sum
   if (tid == kThreads - 1) found[0] = total;
