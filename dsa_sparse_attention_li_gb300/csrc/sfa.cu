@@ -49,8 +49,9 @@
 //
 // FP8 latent cache ("Inference Optimization for Kimi K3.1 Pro", section 4: the cache stored in
 // FP8 per token and 128-column tile, the attention arithmetic in BF16): rows of 576 e4m3 codes
-// and 5 fp32 tile scales; the gather threads load codes and scales, de-quantise in registers
-// (fp32 product, bf16 rounding) and store the same swizzled BF16 tiles, so everything after the
+// and 5 fp32 tile scales; the gather threads copy the codes and scales they need into the upper
+// part of the tile's stage with cp.async, and convert a tile (fp32 product, bf16 rounding) into
+// the same swizzled BF16 tile once the next tile's copies are issued, so everything after the
 // gather is unchanged (template parameter KV8).
 #include <algorithm>
 #include <cmath>
@@ -217,6 +218,11 @@ DSA_DEV uint32_t stage_chunk_offset(int ch, int rr) {
 
 // FP8 latent rows: 576 e4m3 codes, one fp32 scale per 128-column tile (5), padding to 608 B.
 constexpr int kKv8Row = 608;
+// A CTA's part of an FP8 row as staged in the upper part of a ring stage: 256 value codes, 32 rope
+// codes and the row's 32 scale bytes (20 chunks of 16 bytes), 64 rows = 20 KiB.
+constexpr int kKv8Chunks = 20;
+constexpr int kKv8StageRow = 16 * kKv8Chunks;
+constexpr int kKv8Stage = kTileBytes - kNT * kKv8StageRow;  // 16 KiB
 
 // Two e4m3 codes (low byte first) times their tile scale: fp32 products rounded to nearest, then
 // packed as two bf16 rounded to nearest even.
@@ -374,59 +380,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One thread polls each barrier; the other gather warps sleep on a hardware barrier and
     // then read the poller's verdict (bit i & 1 of gather_go, which is not rewritten before
     // every gather thread has passed the next bar.sync, so all of them leave at the same step).
-    for (int i = 0; i < ntile; ++i) {
-      const int s = i % kStages;
-      if (i >= kStages) {
-        // a reused stage waits for the P.V that read it
-        if (g == 0) {
-          const int v = mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status) ? 1 : 0;
-          volatile int* go = &ctl->gather_go;
-          *go = (*go & ~(1 << (i & 1))) | (v << (i & 1));
+    if constexpr (KV8) {
+      // FP8 rows ("Inference Optimization for Kimi K3.1 Pro", section 4: the cache is FP8 with a
+      // scale per token and 128-column tile, the attention arithmetic BF16).  The codes and
+      // scales this CTA uses (320 of a row's 608 bytes: its 256 value codes, 32 rope codes and
+      // the 32 scale bytes) are copied with cp.async into the upper 20 KiB of the tile's stage,
+      // and a tile is converted into the swizzled BF16 operand after the next one has been
+      // issued, so the copies of two tiles are in flight while the threads convert.
+      auto issue = [&](int i, int s) {
+        const uint32_t stg = smem_u32(st_s) + (uint32_t)(s * kTileBytes + kKv8Stage);
+        for (int c = g; c < kNT * kKv8Chunks; c += kGatherThreads) {
+          const int r = c / kKv8Chunks, k = c % kKv8Chunks;
+          const int slot = i * kNT + r;
+          const int row = slot < nslot ? rows_s[slot] : -1;
+          const uint32_t src_off = k < 16 ? (uint32_t)(kDvHalf * half + 16 * k)
+                                 : (k < 18 ? (uint32_t)(kDv + kRopeHalf * half + 16 * (k - 16))
+                                           : (uint32_t)(kDqk + 16 * (k - 18)));
+          const uint8_t* src = row >= 0 ? kv + (size_t)row * kKv8Row + src_off : kv;
+          cp_async16(stg + (uint32_t)(r * kKv8StageRow + 16 * k), src, row >= 0 ? 16u : 0u);
         }
-        named_barrier(1, kGatherThreads);
-        if (((*reinterpret_cast<volatile int*>(&ctl->gather_go) >> (i & 1)) & 1) == 0) break;
-      }
-      const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
-      if constexpr (KV8) {
-        // FP8 rows ("Inference Optimization for Kimi K3.1 Pro", section 4: the cache is FP8
-        // with a scale per token and 128-column tile, the attention arithmetic BF16): each
-        // 16-byte operand chunk is 8 codes of the row times their tile scale, converted in
-        // registers and stored swizzled; empty slots store zeros.  Six chunks' loads in flight.
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      };
+      auto convert = [&](int s, bool newer_pending) {
+        if (newer_pending)
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else
+          asm volatile("cp.async.wait_group 0;" ::: "memory");
+        named_barrier(1, kGatherThreads);  // every thread's copies of tile i have landed
         uint8_t* stage = st_s + (size_t)s * kTileBytes;
+        const uint8_t* stg = stage + kKv8Stage;
+        uint2 code[kGatherPer];
+        float sc[kGatherPer];
 #pragma unroll
-        for (int k0 = 0; k0 < kGatherPer; k0 += 6) {
-          uint2 code[6];
-          float sc[6];
-          uint32_t off[6];
-#pragma unroll
-          for (int u = 0; u < 6; ++u) {
-            const int c = g + (k0 + u) * kGatherThreads;
-            code[u] = make_uint2(0u, 0u);
-            sc[u] = 0.f;
-            off[u] = 0xffffffffu;
-            if (k0 + u < kGatherPer && c < kChunks) {
-              const int r = c / kRowChunks, ch = c % kRowChunks;
-              const int slot = i * kNT + r;
-              const int row = slot < nslot ? rows_s[slot] : -1;
-              off[u] = stage_chunk_offset(ch, r);
-              if (row >= 0) {
-                const int e = row_chunk_offset(ch, half) >> 1;  // first of the chunk's 8 columns
-                const uint8_t* rp = kv + (size_t)row * kKv8Row;
-                code[u] = __ldg(reinterpret_cast<const uint2*>(rp + e));
-                sc[u] = __ldg(reinterpret_cast<const float*>(rp + kDqk + 4 * (e >> 7)));
-              }
-            }
+        for (int k = 0; k < kGatherPer; ++k) {
+          const int c = g + k * kGatherThreads;
+          code[k] = make_uint2(0u, 0u);
+          sc[k] = 0.f;
+          if (c < kChunks) {
+            const int r = c / kRowChunks, ch = c % kRowChunks;
+            const uint8_t* rp = stg + r * kKv8StageRow;
+            const int e = ch < 32 ? 8 * ch : kDvHalf + 8 * (ch - 32);  // first of the 8 codes
+            const int tile = ch < 32 ? 2 * half + ch / 16 : 4;         // their 128-column tile
+            code[k] = *reinterpret_cast<const uint2*>(rp + e);
+            sc[k] = *reinterpret_cast<const float*>(rp + 288 + 4 * tile);
           }
+        }
+        named_barrier(1, kGatherThreads);  // staged bytes are read before the BF16 tile overwrites them
 #pragma unroll
-          for (int u = 0; u < 6; ++u)
-            if (off[u] != 0xffffffffu)
-              *reinterpret_cast<uint4*>(stage + off[u]) =
-                  make_uint4(dequant2(code[u].x & 0xffffu, sc[u]), dequant2(code[u].x >> 16, sc[u]),
-                             dequant2(code[u].y & 0xffffu, sc[u]), dequant2(code[u].y >> 16, sc[u]));
+        for (int k = 0; k < kGatherPer; ++k) {
+          const int c = g + k * kGatherThreads;
+          if (c < kChunks) {
+            const int r = c / kRowChunks, ch = c % kRowChunks;
+            *reinterpret_cast<uint4*>(stage + stage_chunk_offset(ch, r)) =
+                make_uint4(dequant2(code[k].x & 0xffffu, sc[k]), dequant2(code[k].x >> 16, sc[k]),
+                           dequant2(code[k].y & 0xffffu, sc[k]), dequant2(code[k].y >> 16, sc[k]));
+          }
         }
         fence_proxy_async_smem();  // generic-proxy stores -> the tensor core's reads
         mbar_arrive(&ctl->full[s]);
-      } else {
+      };
+      int issued = 0;
+      for (int i = 0; i < ntile; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages) {
+          // a reused stage waits for the P.V that read it
+          if (g == 0) {
+            const int v = mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status) ? 1 : 0;
+            volatile int* go = &ctl->gather_go;
+            *go = (*go & ~(1 << (i & 1))) | (v << (i & 1));
+          }
+          named_barrier(1, kGatherThreads);
+          if (((*reinterpret_cast<volatile int*>(&ctl->gather_go) >> (i & 1)) & 1) == 0) break;
+        }
+        issue(i, s);
+        issued = i + 1;
+        if (i >= 1) convert((i - 1) % kStages, true);
+      }
+      if (issued == ntile && ntile > 0) convert((ntile - 1) % kStages, false);
+    } else {
+      for (int i = 0; i < ntile; ++i) {
+        const int s = i % kStages;
+        if (i >= kStages) {
+          // a reused stage waits for the P.V that read it
+          if (g == 0) {
+            const int v = mbar_wait(&ctl->empty[s], ((uint32_t)(i / kStages) & 1u) ^ 1u, abort, p.status) ? 1 : 0;
+            volatile int* go = &ctl->gather_go;
+            *go = (*go & ~(1 << (i & 1))) | (v << (i & 1));
+          }
+          named_barrier(1, kGatherThreads);
+          if (((*reinterpret_cast<volatile int*>(&ctl->gather_go) >> (i & 1)) & 1) == 0) break;
+        }
+        const uint32_t base = smem_u32(st_s) + (uint32_t)(s * kTileBytes);
 #pragma unroll
         for (int k = 0; k < kGatherPer; ++k) {
           const int c = g + k * kGatherThreads;
