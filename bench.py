@@ -502,7 +502,7 @@ def run_ours(args):
         "step_hbm": {"metric_bytes": work["metric_bytes"], "achieved_gbs": step_gbs,
                      "frac": step_gbs / hbm, "peak_kind": peak_kind},
         "kernels": kernels,
-        "gpu_launches": (3 if li_nb else 2) * K,  # indexer (+ unit merge) + attention per step
+        "gpu_launches": (4 if li_nb else 2) * K,  # indexer (+ unit plan and merge) + attention
         "clocks": clk.summary(),
     }
     if e2e:
