@@ -1127,12 +1127,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // then read their item from the list.  A sequence of L positions has ceil(L / span) units of
 // ceil(L / units) positions.
 __global__ void __launch_bounds__(256) unit_plan_kernel(const int* seq_lens, int B, int span,
-                                                        int* items) {
+                                                        int units, int* items) {
   __shared__ int ulen[kMaxUnitSeqs], ucnt[kMaxUnitSeqs];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < B) {
     const int L = max(0, seq_lens[tid]);
-    const int nu = max(1, (L + span - 1) / span);
+    // (a length beyond units * span is reported by the indexer; the list stays in bounds)
+    const int nu = min(units, max(1, (L + span - 1) / span));
     ulen[tid] = (L + nu - 1) / nu;
     ucnt[tid] = nu;
   }
@@ -1273,7 +1274,7 @@ static dsa_status launch_impl(const dsa_li_args& a, cudaStream_t stream, std::st
     um.cand_idx = reinterpret_cast<int*>(a.workspace);
     um.cand_score = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.workspace) + half);
     items = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(a.workspace) + 2 * half);
-    unit_plan_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.B, best_c * best_chunk, items);
+    unit_plan_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.B, best_c * best_chunk, units, items);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "li_topk: unit plan launch", err);
   }

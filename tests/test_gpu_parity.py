@@ -207,6 +207,25 @@ def test_sequence_longer_than_page_table_sets_status_without_fault(cuda_lib):
     assert int(status.item()) == dsa.DSA_ERR_DEVICE_CHECK
 
 
+def test_unit_length_beyond_bound_sets_status_without_fault(cuda_lib):
+    """With position units, a sequence longer than max_seq_len (units x span) is reported and
+    skipped by the plan, the indexer and the merge; the other sequences are still exact."""
+    inp_cpu, inp = _small("decode_int_4k", seq_lens=[40000, 70000], n_new=[1, 1])
+    wl = inp_cpu["wl"]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.full((wl.n_q, wl.K), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros((wl.n_q,), dtype=torch.int32, device="cuda")
+    assert dsa.li_workspace_bytes(2, wl.K, 40000, 1) > 0
+    dsa.li_topk(inp["q_li"], inp["w"], inp["k_pool"], inp["pt_k"], inp["seq_lens"], inp["q_start"],
+                wl.K, max_seq_len=40000, max_q_per_seq=1, out_idx=idx, out_cnt=cnt, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == dsa.DSA_ERR_DEVICE_CHECK
+    g = {"idx": idx.cpu().numpy(), "cnt": cnt.cpu().numpy()}
+    n_exact, _ = check_indices(inp_cpu, g, [0], exact=True)
+    assert n_exact == 1
+    assert np.all(g["idx"][1] == -7)  # the skipped token's row is left as it was
+
+
 def test_cache_write_roundtrip(cuda_lib):
     inp_cpu, inp = _small("decode_32k", seq_lens=[200, 100], n_new=[1, 1])
     pool = torch.zeros_like(inp["kv_pool"])
