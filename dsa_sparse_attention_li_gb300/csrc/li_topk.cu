@@ -1013,106 +1013,150 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ascending-position compaction: ties at the threshold go to the lowest positions.  A warp
   // stages its selected positions in place at the front of its own segment of the key array
-  // (never ahead of what it has read), then writes them out with coalesced stores.
-#pragma unroll 1
-  for (int tt = 0; tt < nt; ++tt) {
-    const bool radix = ctl->radix[tt] != 0;
-    const uint32_t thr = radix ? ctl->prefix[tt] : 0u;
-    const int need_total = ctl->need_total[tt];
-    int eq_before = 0, off = ctl->offset[tt];
-    for (int w = 0; w < warp; ++w) {
-      const int ties_w = max(0, min(ctl->weq[tt][w], ctl->quota[tt] - eq_before));
-      off += ctl->wgt[tt][w] + ties_w;
-      eq_before += ctl->weq[tt][w];
-    }
-    const int my_ties = max(0, min(ctl->weq[tt][warp], ctl->quota[tt] - eq_before));
-    const size_t slot_u = ((size_t)(b * p.groups + g) * p.units + unit) * T + tt;
-    int* out = direct ? p.out_idx + (size_t)(t0 + tt) * p.K : p.cand_idx + slot_u * p.K;
-    float* out_sc = direct ? (p.out_score ? p.out_score + (size_t)(t0 + tt) * p.K : nullptr)
+  // (never ahead of what it has read), then writes them out with coalesced stores.  The tokens
+  // of a group go through each 512-key batch together, so their latency chains overlap.
+  {
+    int off_t[T], ties_t[T], need_t[T], eqr_t[T], selr_t[T];
+    uint32_t thr_t[T];
+    bool rdx_t[T];
+    int* out_t[T];
+    float* osc_t[T];
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt) {
+      off_t[tt] = ties_t[tt] = need_t[tt] = eqr_t[tt] = selr_t[tt] = 0;
+      thr_t[tt] = 0u;
+      rdx_t[tt] = false;
+      out_t[tt] = nullptr;
+      osc_t[tt] = nullptr;
+      if (tt < nt) {
+        rdx_t[tt] = ctl->radix[tt] != 0;
+        thr_t[tt] = rdx_t[tt] ? ctl->prefix[tt] : 0u;
+        need_t[tt] = ctl->need_total[tt];
+        int eq_before = 0, off = ctl->offset[tt];
+        for (int w = 0; w < warp; ++w) {
+          const int ties_w = max(0, min(ctl->weq[tt][w], ctl->quota[tt] - eq_before));
+          off += ctl->wgt[tt][w] + ties_w;
+          eq_before += ctl->weq[tt][w];
+        }
+        off_t[tt] = off;
+        ties_t[tt] = max(0, min(ctl->weq[tt][warp], ctl->quota[tt] - eq_before));
+        const size_t slot_u = ((size_t)(b * p.groups + g) * p.units + unit) * T + tt;
+        out_t[tt] = direct ? p.out_idx + (size_t)(t0 + tt) * p.K : p.cand_idx + slot_u * p.K;
+        osc_t[tt] = direct ? (p.out_score ? p.out_score + (size_t)(t0 + tt) * p.K : nullptr)
                            : p.cand_score + slot_u * p.K;
-    uint32_t* sc = scores + tt * p.chunk;
-    int eq_run = 0, sel_run = 0;
+      }
+    }
     // batches of four 128-key groups: lane holds keys 4*lane..4*lane+3 of each group
 #pragma unroll 1
     for (int eb = e_lo; eb < e_hi; eb += 512) {
-      uint32_t key[16];
-      uint32_t take = 0, feq = 0;
+      uint32_t key[T][16], take[T], feq[T], tinc[T], tcnt[T];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (eb + 128 * g < e_hi) v = *reinterpret_cast<const uint4*>(sc + eb + 128 * g + 4 * lane);
-        key[4 * g + 0] = v.x; key[4 * g + 1] = v.y; key[4 * g + 2] = v.z; key[4 * g + 3] = v.w;
+      for (int tt = 0; tt < T; ++tt) {
+        take[tt] = feq[tt] = 0u;
+        if (tt < nt) {
+          const uint32_t* sc = scores + tt * p.chunk;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t u = key[4 * g + k];
-          if (u > thr) take |= 1u << (4 * g + k);
-          if (radix && u == thr && u != 0u) feq |= 1u << (4 * g + k);
-        }
-      }
-      if (__any_sync(0xffffffffu, feq != 0u)) {
-        // keys equal to the threshold: this warp takes the first my_ties of them
-        const uint32_t ecnt = nibble_counts(feq);
-        const uint32_t einc = warp_incl_scan(ecnt);
-        const uint32_t etot = __shfl_sync(0xffffffffu, einc, 31);
-        const uint32_t eexc = einc - ecnt;
-        int ebase = eq_run;
+          for (int gg = 0; gg < 4; ++gg) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (eb + 128 * gg < e_hi) v = *reinterpret_cast<const uint4*>(sc + eb + 128 * gg + 4 * lane);
+            key[tt][4 * gg + 0] = v.x; key[tt][4 * gg + 1] = v.y;
+            key[tt][4 * gg + 2] = v.z; key[tt][4 * gg + 3] = v.w;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          int seen = ebase + (int)((eexc >> (8 * g)) & 0xffu);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if ((feq >> (4 * g + k)) & 1u) {
-              if (seen < my_ties) take |= 1u << (4 * g + k);
-              ++seen;
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t u = key[tt][4 * gg + k];
+              if (u > thr_t[tt]) take[tt] |= 1u << (4 * gg + k);
+              if (rdx_t[tt] && u == thr_t[tt] && u != 0u) feq[tt] |= 1u << (4 * gg + k);
             }
-          ebase += (int)((etot >> (8 * g)) & 0xffu);
-        }
-        eq_run = ebase;
-      }
-      const uint32_t tcnt = nibble_counts(take);
-      const uint32_t tinc = warp_incl_scan(tcnt);
-      const uint32_t ttot = __shfl_sync(0xffffffffu, tinc, 31);
-      const uint32_t texc = tinc - tcnt;
-      // every lane's keys of the batch are in registers (the scan above), and the staged count
-      // never exceeds the keys read so far: the writes land on keys already consumed
-      int base = sel_run;
-      if (out_sc == nullptr) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if ((take >> (4 * g + k)) & 1u) sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
-          base += (int)((ttot >> (8 * g)) & 0xffu);
-        }
-      } else {  // also the score of each selected position (uncoalesced; optional output)
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          int slot = e_lo + base + (int)((texc >> (8 * g)) & 0xffu);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if ((take >> (4 * g + k)) & 1u) {
-              if (off + (slot - e_lo) < need_total) out_sc[off + (slot - e_lo)] = key_score(key[4 * g + k]);
-              sc[slot++] = (uint32_t)(lo + eb + 128 * g + 4 * lane + k);
-            }
-          base += (int)((ttot >> (8 * g)) & 0xffu);
+          }
         }
       }
-      sel_run = base;
+#pragma unroll
+      for (int tt = 0; tt < T; ++tt) {
+        if (tt < nt && __any_sync(0xffffffffu, feq[tt] != 0u)) {
+          // keys equal to the threshold: this warp takes the first ties_t of them
+          const uint32_t ecnt = nibble_counts(feq[tt]);
+          const uint32_t einc = warp_incl_scan(ecnt);
+          const uint32_t etot = __shfl_sync(0xffffffffu, einc, 31);
+          const uint32_t eexc = einc - ecnt;
+          int ebase = eqr_t[tt];
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            int seen = ebase + (int)((eexc >> (8 * gg)) & 0xffu);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if ((feq[tt] >> (4 * gg + k)) & 1u) {
+                if (seen < ties_t[tt]) take[tt] |= 1u << (4 * gg + k);
+                ++seen;
+              }
+            ebase += (int)((etot >> (8 * gg)) & 0xffu);
+          }
+          eqr_t[tt] = ebase;
+        }
+      }
+      // the tokens' packed warp scans, step by step
+#pragma unroll
+      for (int tt = 0; tt < T; ++tt) tinc[tt] = tcnt[tt] = nibble_counts(take[tt]);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, tinc[tt], o);
+          if (lane >= o) tinc[tt] += y;
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < T; ++tt) {
+        if (tt >= nt) continue;
+        uint32_t* sc = scores + tt * p.chunk;
+        const uint32_t ttot = __shfl_sync(0xffffffffu, tinc[tt], 31);
+        const uint32_t texc = tinc[tt] - tcnt[tt];
+        // every lane's keys of the batch are in registers (the scan above), and the staged
+        // count never exceeds the keys read so far: the writes land on keys already consumed
+        int base = selr_t[tt];
+        if (osc_t[tt] == nullptr) {
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            int slot = e_lo + base + (int)((texc >> (8 * gg)) & 0xffu);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if ((take[tt] >> (4 * gg + k)) & 1u) sc[slot++] = (uint32_t)(lo + eb + 128 * gg + 4 * lane + k);
+            base += (int)((ttot >> (8 * gg)) & 0xffu);
+          }
+        } else {  // also the score of each selected position (uncoalesced; optional output)
+#pragma unroll
+          for (int gg = 0; gg < 4; ++gg) {
+            int slot = e_lo + base + (int)((texc >> (8 * gg)) & 0xffu);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if ((take[tt] >> (4 * gg + k)) & 1u) {
+                if (off_t[tt] + (slot - e_lo) < need_t[tt])
+                  osc_t[tt][off_t[tt] + (slot - e_lo)] = key_score(key[tt][4 * gg + k]);
+                sc[slot++] = (uint32_t)(lo + eb + 128 * gg + 4 * lane + k);
+              }
+            base += (int)((ttot >> (8 * gg)) & 0xffu);
+          }
+        }
+        selr_t[tt] = base;
+      }
     }
     __syncwarp();
-    for (int j = lane; j < sel_run; j += 32) {
-      if (off + j < need_total)
-        out[off + j] = (int)sc[e_lo + j];
-      else
-        report(p.status, kStatusDeviceCheck);
-    }
-    if (rank == 0) {
-      for (int r = need_total + tid; r < p.K; r += kThreads) {
-        out[r] = -1;
-        if (out_sc) out_sc[r] = -INFINITY;
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt) {
+      if (tt >= nt) continue;
+      const uint32_t* sc = scores + tt * p.chunk;
+      for (int j = lane; j < selr_t[tt]; j += 32) {
+        if (off_t[tt] + j < need_t[tt])
+          out_t[tt][off_t[tt] + j] = (int)sc[e_lo + j];
+        else
+          report(p.status, kStatusDeviceCheck);
       }
-      if (direct && tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_total;
+      if (rank == 0) {
+        for (int r = need_t[tt] + tid; r < p.K; r += kThreads) {
+          out_t[tt][r] = -1;
+          if (osc_t[tt]) osc_t[tt][r] = -INFINITY;
+        }
+        if (direct && tid == 0 && p.out_cnt) p.out_cnt[t0 + tt] = need_t[tt];
+      }
     }
   }
   // peers may still be reading this CTA's counters / candidates
