@@ -142,6 +142,7 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
   uint32_t scan[kThreads / 32];
+  uint32_t scan_t[4][kThreads / 32];  // per-token block scans
   int need[4];        // remaining count to select among the current prefix
   uint32_t prefix[4]; // key prefix fixed so far
   int radix[4];       // token needs a radix select (visible > K)
@@ -180,6 +181,38 @@ DSA_DEV uint32_t block_excl_suffix(uint32_t v, uint32_t* scratch) {
     if (w > warp) above += scratch[w];
   __syncthreads();
   return above + x - v;
+}
+
+// The same for NT values per thread at once (one pair of block barriers for all of them).
+template <int NT>
+DSA_DEV void block_excl_suffix_multi(const uint32_t (&v)[NT], uint32_t (*scratch)[kThreads / 32],
+                                     uint32_t (&above)[NT]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) x[n] = v[n];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, x[n], o);
+      if (lane + o < 32) x[n] += y;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) scratch[n][warp] = x[n];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    uint32_t a = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w)
+      if (w > warp) a += scratch[n][w];
+    above[n] = a + x[n] - v[n];
+  }
+  __syncthreads();
 }
 
 // Adds the 8 packed 16-bit bins of histogram words h[0..3] of every CTA of the cluster (C CTAs)
@@ -590,41 +623,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool fast = false;
   if (any_radix) {
     cluster_sync();
-#pragma unroll 1
-    for (int tt = 0; tt < T; ++tt) {
-      if (!ctl->radix[tt]) continue;  // uniform over the block
-      uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (tid < kHistThreads) {
-        const uint32_t* h = hist + tt * kHistWords + 4 * tid;
-        cluster_hist_sum(h, p.C, cnt);
-      }
-      uint32_t sum = 0;
+    // every token of the group at once: its 2048 bins summed over the cluster, then one block
+    // scan per token (sharing the barriers) finds the bin that holds its K-th key
+    uint32_t cnt[T][8], sum[T], above[T];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sum += cnt[k];
-      if (tid == 0) {
-        ctl->found_bin[tt] = 0;
-        ctl->found_need[tt] = 1;
-        ctl->cand_total[tt] = 0x7fffffff;
-      }
-      const uint32_t above = block_excl_suffix(sum, ctl->scan);
+    for (int tt = 0; tt < T; ++tt) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) cnt[tt][k] = 0u;
+      if (tid < kHistThreads && ctl->radix[tt]) cluster_hist_sum(hist + tt * kHistWords + 4 * tid, p.C, cnt[tt]);
+      sum[tt] = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum[tt] += cnt[tt][k];
+    }
+    if (tid < T) {
+      ctl->found_bin[tid] = 0;
+      ctl->found_need[tid] = 1;
+      ctl->cand_total[tid] = 0x7fffffff;
+    }
+    block_excl_suffix_multi<T>(sum, ctl->scan_t, above);
+#pragma unroll
+    for (int tt = 0; tt < T; ++tt) {
+      if (!ctl->radix[tt]) continue;
       const uint32_t need = (uint32_t)ctl->need[tt];
-      uint32_t run = above;
+      uint32_t run = above[tt];
 #pragma unroll
       for (int k = 7; k >= 0; --k) {
-        if (run < need && run + cnt[k] >= need) {
+        if (run < need && run + cnt[tt][k] >= need) {
           ctl->found_bin[tt] = 8 * tid + k;
           ctl->found_need[tt] = (int)(need - run);
-          ctl->cand_total[tt] = (int)cnt[k];
+          ctl->cand_total[tt] = (int)cnt[tt][k];
         }
-        run += cnt[k];
+        run += cnt[tt][k];
       }
-      __syncthreads();
-      if (tid == 0) {
-        ctl->prefix[tt] = (uint32_t)ctl->found_bin[tt] << 21;
-        ctl->need[tt] = ctl->found_need[tt];
-      }
-      __syncthreads();
     }
+    __syncthreads();
+    if (tid < T && ctl->radix[tid]) {
+      ctl->prefix[tid] = (uint32_t)ctl->found_bin[tid] << 21;
+      ctl->need[tid] = ctl->found_need[tid];
+    }
+    __syncthreads();
     // Candidate path when every threshold bin is small enough to gather into one CTA.
     const int cap = p.nstage * CF::kTileBytes / 2 / 8 / T;
     // a lane's candidate bits (4 per 128-key step of its warp segment) fit one 64-bit word
@@ -679,32 +716,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       cbits[tt] = 0ull;
       lane_base[tt] = 0;
     }
+    {
+      // the tokens of the group scan the warp's segment together
+      bool rdx[T];
+      uint32_t b0[T], sure[T];
+      uint64_t bits[T];
 #pragma unroll
-    for (int tt = 0; tt < T; ++tt) {
-      const bool rdx = ctl->radix[tt] != 0;
-      const uint32_t b0 = ctl->prefix[tt] >> 21;
-      const uint32_t* sc = scores + tt * p.chunk;
-      uint32_t sure = 0;
-      uint64_t bits = 0ull;
+      for (int tt = 0; tt < T; ++tt) {
+        rdx[tt] = ctl->radix[tt] != 0;
+        b0[tt] = ctl->prefix[tt] >> 21;
+        sure[tt] = 0u;
+        bits[tt] = 0ull;
+      }
 #pragma unroll 2
       for (int e = e_lo + 4 * lane, it = 0; e < e_hi; e += 128, ++it) {
-        const uint4 v = *reinterpret_cast<const uint4*>(sc + e);
-        const uint32_t us[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          sure += rdx ? ((us[k] >> 21) > b0) : (us[k] != 0u);
-          if (rdx && us[k] != 0u && (us[k] >> 21) == b0) bits |= 1ull << (4 * it + k);
+        for (int tt = 0; tt < T; ++tt) {
+          const uint4 v = *reinterpret_cast<const uint4*>(scores + tt * p.chunk + e);
+          const uint32_t us[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            sure[tt] += rdx[tt] ? ((us[k] >> 21) > b0[tt]) : (us[k] != 0u);
+            if (rdx[tt] && us[k] != 0u && (us[k] >> 21) == b0[tt]) bits[tt] |= 1ull << (4 * it + k);
+          }
         }
       }
-      const uint32_t mine = (uint32_t)__popcll(bits);
-      const uint32_t inc = warp_incl_scan(mine);
-      cbits[tt] = bits;
-      lane_base[tt] = (int)(inc - mine);
-      sure = __reduce_add_sync(0xffffffffu, sure);
-      const uint32_t cand = __shfl_sync(0xffffffffu, inc, 31);
-      if (lane == 0) {
-        ctl->wgt[tt][warp] = (int)sure;
-        ctl->wcnd[tt][warp] = (int)cand;
+      uint32_t mine[T], inc[T];
+#pragma unroll
+      for (int tt = 0; tt < T; ++tt) inc[tt] = mine[tt] = (uint32_t)__popcll(bits[tt]);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, inc[tt], o);
+          if (lane >= o) inc[tt] += y;
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < T; ++tt) {
+        cbits[tt] = bits[tt];
+        lane_base[tt] = (int)(inc[tt] - mine[tt]);
+        const uint32_t sr = __reduce_add_sync(0xffffffffu, sure[tt]);
+        const uint32_t cand = __shfl_sync(0xffffffffu, inc[tt], 31);
+        if (lane == 0) {
+          ctl->wgt[tt][warp] = (int)sr;
+          ctl->wcnd[tt][warp] = (int)cand;
+        }
       }
     }
     __syncthreads();
