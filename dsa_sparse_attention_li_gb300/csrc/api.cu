@@ -255,7 +255,7 @@ static dsa_status prolog_check(const dsa_prolog_args* a, bool pointers) {
   if (!pointers) return DSA_OK;  // sizes only (workspace query)
   if (!a->xq || !a->x || !a->w_q || !a->w_k || !a->w_w || !a->ln_gamma || !a->ln_beta ||
       !a->page_table || !a->seq_lens || !a->q_start || !a->q_out || !a->w_out || !a->k_pool ||
-      !a->workspace || (a->dtype == DSA_MXFP8_E4M3 && (!a->q_sf || !a->k_sf)))
+      (a->dtype == DSA_MXFP8_E4M3 && (!a->q_sf || !a->k_sf)))
     return fail(DSA_ERR_INVALID_ARG, "indexer_prolog: null device pointer");
   if (!aligned16(a->xq) || !aligned16(a->x) || !aligned16(a->w_q) || !aligned16(a->w_k) ||
       !aligned16(a->w_w))

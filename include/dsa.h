@@ -302,14 +302,15 @@ typedef struct {
   float* w_out;         /* [n_q][H_I]                                                      */
   void* k_pool;         /* [num_pages][page_size][d_I] e4m3 codes or bf16 (written rows only) */
   uint8_t* k_sf;        /* [num_pages][page_size][d_I/32] (MXFP8)                          */
-  void* workspace;      /* dsa_prolog_workspace_bytes() bytes, zeroed once before first use;
-                           a call leaves its counters at zero again (not after a timeout)  */
+  void* workspace;      /* unused: dsa_prolog_workspace_bytes() is 0 (the slices of a tile
+                           meet in distributed shared memory); may be NULL                */
   size_t workspace_bytes;
   int32_t* status;      /* device int32 error word, or NULL                                */
 } dsa_prolog_args;
 
-/* Scratch bytes dsa_indexer_prolog needs for these sizes on the current device (only the size
- * fields are read; 0 if they are invalid). */
+/* Scratch bytes dsa_indexer_prolog needs for these sizes (only the size fields are read): 0 --
+ * this implementation needs none; kept so that callers size the field the same way as the
+ * other entry points' workspaces. */
 size_t dsa_prolog_workspace_bytes(const dsa_prolog_args* args);
 dsa_status dsa_indexer_prolog(const dsa_prolog_args* args, dsa_stream_t stream);
 
