@@ -294,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const Params p) {
   using CF = Cfg<D_I, FP8, H_I, T, MX>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so that the compiler
+  // keeps the accesses through it in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Layout lay(p.nstage, CF::kTileBytes, CF::kQBytes, T, H_I, p.chunk);
   uint8_t* stage_base = smem + lay.stages;
   uint8_t* q_s = smem + lay.q;

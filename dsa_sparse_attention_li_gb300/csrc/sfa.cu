@@ -252,8 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sfa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
                const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so that the compiler
+  // keeps the accesses through it in the shared state space
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* st_s = smem + Layout::stages;
   uint4* xbuf = reinterpret_cast<uint4*>(smem + Layout::xbuf);
   int* rows_s = reinterpret_cast<int*>(smem + Layout::rows);
