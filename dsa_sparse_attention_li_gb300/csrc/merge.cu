@@ -135,14 +135,36 @@ __global__ void __launch_bounds__(kThreads)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ uint32_t hist[2048];
   __shared__ uint32_t wsum[32];
-  __shared__ uint32_t found[2];
+  __shared__ uint32_t found[3];
+  __shared__ int bsel[5];  // the token's sequence: index, matching ranges, length, range
   uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);   // [units * K] score keys, 0 = none
   int* pos = reinterpret_cast<int*>(key + a.units * a.K);  // [units * K]
-  griddep_wait();
   const int t = blockIdx.x, tid = threadIdx.x;
-  const int b = find_seq(a.q_start, a.B, t);
-  const int qs = a.q_start[b], n_b = a.q_start[b + 1] - qs;
-  const int L = a.seq_lens[b];
+  if (tid == 0) {
+    bsel[0] = -1;
+    bsel[1] = 0;
+  }
+  __syncthreads();
+  griddep_wait();
+  // the token's sequence in one round of loads (every thread tests one sequence's range)
+  for (int i = tid; i < a.B; i += kThreads) {
+    const int s0 = a.q_start[i], s1 = a.q_start[i + 1], len = a.seq_lens[i];
+    if (s0 <= t && t < s1) {
+      atomicMax(&bsel[0], i);
+      atomicAdd(&bsel[1], 1);
+      bsel[2] = len;
+      bsel[3] = s0;
+      bsel[4] = s1;
+    }
+  }
+  __syncthreads();
+  int b = bsel[0], qs = bsel[3], n_b = bsel[4] - bsel[3], L = bsel[2];
+  if (bsel[1] != 1) {  // q_start not increasing, or t outside it: the largest b with q_start[b] <= t
+    b = find_seq(a.q_start, a.B, t);
+    qs = a.q_start[b];
+    n_b = a.q_start[b + 1] - qs;
+    L = a.seq_lens[b];
+  }
   // the indexer reported (and skipped) a sequence that fails these
   if (n_b <= 0 || L < n_b || L > a.units * a.span || L > a.max_pages * 64 || qs < 0 ||
       qs + n_b > a.n_q || n_b > a.groups * a.T || t - qs >= n_b)
@@ -151,10 +173,11 @@ __global__ void __launch_bounds__(kThreads)
   if (n_u <= 1) return;  // the indexer wrote this token's result
   const int g = (t - qs) / a.T, tt = (t - qs) % a.T;
   const int ncand = n_u * a.K;
-  // every load of a thread in flight at once: units x ceil(K / threads) <= 16 pairs
-  uint32_t nvalid = 0;
+  // every load of a thread in flight at once: units x ceil(K / threads) <= 16 pairs; the keys
+  // stay in registers for the three radix passes, the first of which is counted right here
+  constexpr int kPer = kMaxCand / kThreads;
+  uint32_t kr[kPer];
   {
-    constexpr int kPer = kMaxCand / kThreads;
     int jv[kPer];
     float sv[kPer];
 #pragma unroll
@@ -172,61 +195,74 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int i = tid + k * kThreads;
+      // score_key of a finite score is never 0
+      kr[k] = (i < ncand && jv[k] >= 0) ? score_key(sv[k]) : 0u;
       if (i < ncand) {
-        // score_key of a finite score is never 0
-        key[i] = jv[k] >= 0 ? score_key(sv[k]) : 0u;
+        key[i] = kr[k];
         pos[i] = jv[k];
-        nvalid += jv[k] >= 0;
       }
     }
   }
-  const uint32_t total = block_excl_scan(nvalid, wsum) + nvalid;  // the last thread's is the sum
-  if (tid == kThreads - 1) found[0] = total;
+  // first pass (bits 31..21): the candidates are the units' top scores, so most share a few
+  // high bins; the lanes of a warp that hit the same bin add their count with one atomic
+  for (int i = tid; i < 2048; i += kThreads) hist[i] = 0u;
   __syncthreads();
-  const uint32_t all = found[0];
-  const uint32_t cnt = min(all, (uint32_t)a.K);
-  uint32_t thr = 0u, need_eq = 0u;  // take keys > thr, and the first need_eq keys == thr
-  if (all > (uint32_t)a.K) {
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    if (k * kThreads >= ncand) break;  // uniform
+    const uint32_t bin = kr[k] != 0u ? kr[k] >> 21 : 0xffffffffu;
+    const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+    if (kr[k] != 0u && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  }
+  __syncthreads();
+  // Radix select of the K-th largest key: a pass finds the bin that holds it among the keys
+  // that share the prefix fixed so far (thread i owns bins 2p + 1 and 2p with p = 1023 - i: the
+  // exclusive prefix sum counts the keys in higher bins); passes 2 and 3 count only those keys,
+  // from the registers.  The first pass also yields the number of valid candidates.
+  uint32_t all = 0u, thr = 0u, need_eq = 0u;  // take keys > thr, and the first need_eq keys == thr
+  {
     uint32_t prefix = 0u, pmask = 0u, need = (uint32_t)a.K;
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-      const int nbins = pass == 2 ? 1024 : 2048;
-      const uint32_t bmask = (uint32_t)nbins - 1u;
-      for (int i = tid; i < 2048; i += kThreads) hist[i] = 0u;
-      __syncthreads();
-      // The candidates are the units' top scores: most share a few high bins, so the lanes of a
-      // warp that hit the same bin add their count with one atomic.
-      for (int i0 = 0; i0 < ncand; i0 += kThreads) {
-        const int i = i0 + tid;
-        const uint32_t k = i < ncand ? key[i] : 0u;
-        const bool hit = k != 0u && (k & pmask) == prefix;
-        const uint32_t bin = hit ? (k >> shift) & bmask : 0xffffffffu;
-        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-        if (hit && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+      const uint32_t bmask = pass == 2 ? 1023u : 2047u;
+      if (pass > 0) {
+        for (int i = tid; i < 2048; i += kThreads) hist[i] = 0u;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+          if (kr[k] != 0u && (kr[k] & pmask) == prefix) atomicAdd(&hist[(kr[k] >> shift) & bmask], 1u);
+        __syncthreads();
       }
-      __syncthreads();
-      // thread i owns bins 2p + 1 and 2p with p = 1023 - i: the exclusive prefix sum counts the
-      // keys in higher bins
       const int pr = 1023 - tid;
       const uint32_t c_hi = hist[2 * pr + 1], c_lo = hist[2 * pr];
       const uint32_t above = block_excl_scan(c_hi + c_lo, wsum);
+      if (pass == 0 && tid == kThreads - 1) found[1] = above + c_hi + c_lo;  // every key
       if (above < need && above + c_hi >= need) {
         found[0] = (uint32_t)(2 * pr + 1);
-        found[1] = need - above;
+        found[1 + (pass == 0)] = need - above;
       } else if (above + c_hi < need && above + c_hi + c_lo >= need) {
         found[0] = (uint32_t)(2 * pr);
-        found[1] = need - above - c_hi;
+        found[1 + (pass == 0)] = need - above - c_hi;
       }
       __syncthreads();
+      if (pass == 0) {
+        all = found[1];
+        if (all <= (uint32_t)a.K) break;  // uniform: every candidate is taken
+        need = found[2];
+      } else {
+        need = found[1];
+      }
       prefix |= found[0] << shift;
-      need = found[1];
       pmask |= bmask << shift;
       __syncthreads();
     }
-    thr = prefix;
-    need_eq = need;
+    if (all > (uint32_t)a.K) {
+      thr = prefix;
+      need_eq = need;
+    }
   }
+  const uint32_t cnt = min(all, (uint32_t)a.K);
   // ordered compaction: thread i takes the contiguous run [i * per, (i + 1) * per)
   const int per = (ncand + kThreads - 1) / kThreads;
   const int c0 = min(ncand, tid * per), c1 = min(ncand, c0 + per);

@@ -162,6 +162,7 @@ struct Ctl {
   int abort;
   int nvalid;          // rows up to the last valid slot; at the end: this CTA merges the splits
   int gather_go;       // the gather poller's verdict of step i in bit i & 1
+  int bseq, bcnt, blen;  // the token's sequence: index, ranges that held the token, its length
 };
 static_assert(sizeof(Ctl) <= 512, "control block");
 
@@ -306,6 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     ctl->nvalid = 0;
     ctl->gather_go = 0;
+    ctl->bseq = -1;
+    ctl->bcnt = 0;
+    ctl->blen = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -318,11 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // launch): everything above touches only this CTA's resources; no global memory is read
   // before the preceding kernel has completed and its writes are visible.
   griddep_wait();
-  const int b_seq = find_seq(p.q_start, p.B, t);
-  const int L = min(p.seq_lens[b_seq], p.max_pages * 64);  // positions the page table covers
   if (warp == kMmaWarp && lane == 0 && nslot > 0) {
     // value columns of Q[:, D_r] -> shared memory (moved into TMEM by warps 12-15); issued before
-    // the row translation below so the load overlaps it
+    // the sequence lookup and the row translation below so the load overlaps them
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_qr);
     mbar_arrive_expect_tx(&ctl->qbar, 4 * kHeads * 128 + kHeads * kRopeHalf * 2);
@@ -331,6 +333,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                   (4 * half + bx) * 64, t * p.H);
     tma_load_2d(smem + Layout::qrope, &tm_qr, &ctl->qbar, kDv + kRopeHalf * half, t * p.H);
   }
+  // the token's sequence in one round of loads: every thread tests one sequence's range of
+  // tokens (a binary search over q_start is a chain of dependent loads).  The FP8-cache
+  // instantiation runs at the register limit, where the lookup's extra live state cost more
+  // (spills in the gather loop) than its saved loads, so it keeps the search.
+  int b_seq, len_b;
+  if constexpr (!KV8) {
+    for (int i = tid; i < p.B; i += kThreads) {
+      const int s0 = p.q_start[i], s1 = p.q_start[i + 1], len = p.seq_lens[i];
+      if (s0 <= t && t < s1) {
+        atomicMax(&ctl->bseq, i);
+        atomicAdd(&ctl->bcnt, 1);
+        ctl->blen = len;
+      }
+    }
+    __syncthreads();
+    b_seq = ctl->bseq;
+    len_b = ctl->blen;
+  }
+  if (KV8 || ctl->bcnt != 1) {  // (or q_start not increasing, or t outside it) the largest b with
+                                // q_start[b] <= t
+    b_seq = find_seq(p.q_start, p.B, t);
+    len_b = p.seq_lens[b_seq];
+  }
+  const int L = min(len_b, p.max_pages * 64);  // positions the page table covers
   // logical position -> physical row of every slot of this split (-1: empty or invalid)
   // (all index loads of a thread first, then all page-table loads: two round trips)
   int last_valid = -1;
