@@ -348,15 +348,18 @@ __global__ void __launch_bounds__(kThreads)
       }
       v[b] = acc;
     }
-    if (role == 1) {  // LayerNorm statistics of each row over its 128 features
+    if (role == 1) {  // LayerNorm statistics of each row over its 128 features (rows of the
+                      // batch that do not exist are skipped: rv is warpgroup-uniform)
 #pragma unroll
       for (int b = 0; b < kRowBatch; ++b) {
+        if (!rv[b]) continue;
         const float s = warp_sum(v[b]);
         if (lane == 0) ctl->red[0][warp][b] = s;
       }
       wg_barrier(wg);
 #pragma unroll
       for (int b = 0; b < kRowBatch; ++b) {
+        if (!rv[b]) continue;
         const float mean = (ctl->red[0][wg * 4][b] + ctl->red[0][wg * 4 + 1][b] + ctl->red[0][wg * 4 + 2][b] +
                             ctl->red[0][wg * 4 + 3][b]) * (1.f / 128.f);
         v[b] -= mean;
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(kThreads)
       wg_barrier(wg);
 #pragma unroll
       for (int b = 0; b < kRowBatch; ++b) {
+        if (!rv[b]) continue;
         const float var = (ctl->red[1][wg * 4][b] + ctl->red[1][wg * 4 + 1][b] + ctl->red[1][wg * 4 + 2][b] +
                            ctl->red[1][wg * 4 + 3][b]) * (1.f / 128.f);
         v[b] = v[b] * __frsqrt_rn(var + p.ln_eps) * ln_g + ln_b;
