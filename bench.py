@@ -112,13 +112,17 @@ class ClockSampler:
                 self.samples.append(c.value)
             if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(r)) == 0:
                 self.reasons |= r.value
+            self._first.set()
             time.sleep(0.0005)
 
     def __enter__(self):
         if self.ok:
             self._stop = threading.Event()
+            self._first = threading.Event()
             self._t = threading.Thread(target=self._poll, daemon=True)
             self._t.start()
+            self._first.wait(1.0)  # polling has begun before the caller's timed region starts
+        self.n_start = len(self.samples)
         return self
 
     def __exit__(self, *a):
@@ -128,13 +132,14 @@ class ClockSampler:
 
     def mark(self):
         """Record how many samples the first window (the timed region) holds."""
-        self.n_first = len(self.samples)
+        self.n_first = len(self.samples) - self.n_start
 
     def summary(self):
-        if not self.ok or not self.samples:
+        used = self.samples[getattr(self, "n_start", 0):]  # from the start of the caller's window
+        if not self.ok or not used:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"]}
-        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-               "samples": len(self.samples),
+        out = {"sm_mhz": statistics.median(used), "sm_max_mhz": self.max_mhz,
+               "samples": len(used),
                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b]}
         if getattr(self, "n_first", None) is not None:
             out["samples_timed_region"] = self.n_first
