@@ -407,8 +407,8 @@ def prolog_workspace_bytes(inp: dict) -> int:
 def indexer_prolog(inp: dict, *, q_out=None, q_sf=None, w_out=None, workspace=None, status=None,
                    stream=None):
     """Indexer Prolog of the new tokens: returns (q, q_sf or None, w) and writes the new keys into
-    inp["k_pool"] (and inp["k_sf"]).  ``workspace``: a zeroed uint8 device tensor of
-    prolog_workspace_bytes(inp) bytes (allocated here when not given)."""
+    inp["k_pool"] (and inp["k_sf"]).  ``workspace``: optional; prolog_workspace_bytes(inp) is 0
+    (the input slices of a tile meet in distributed shared memory)."""
     lib = load()
     n_q, H_I, d_I = inp["xq"].shape[0], inp["w_w"].shape[0], inp["w_k"].shape[0]
     dev = inp["xq"].device
@@ -420,8 +420,9 @@ def indexer_prolog(inp: dict, *, q_out=None, q_sf=None, w_out=None, workspace=No
         q_sf = torch.empty((n_q, H_I, d_I // 32), dtype=torch.uint8, device=dev)
     if w_out is None:
         w_out = torch.empty((n_q, H_I), dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = torch.zeros(max(prolog_workspace_bytes(inp), 256), dtype=torch.uint8, device=dev)
+    nb = prolog_workspace_bytes(inp)
+    if workspace is None and nb:
+        workspace = torch.zeros(nb, dtype=torch.uint8, device=dev)
     a = prolog_args(inp, q_out=q_out, q_sf=q_sf, w_out=w_out, workspace=workspace, status=status)
     _check(lib.dsa_indexer_prolog(ctypes.byref(a), _stream(stream)), "dsa_indexer_prolog")
     return q_out, q_sf, w_out
