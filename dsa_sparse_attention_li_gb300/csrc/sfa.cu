@@ -333,6 +333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                   (4 * half + bx) * 64, t * p.H);
     tma_load_2d(smem + Layout::qrope, &tm_qr, &ctl->qbar, kDv + kRopeHalf * half, t * p.H);
   }
+  // this split's selected positions: their loads are in flight during the sequence lookup
+  constexpr int kPer = kMaxRows / kThreads;
+  int j[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = u * kThreads + tid;
+    j[u] = i < nslot ? p.idx[(size_t)t * p.K + slot0 + i] : -1;
+  }
   // the token's sequence in one round of loads: every thread tests one sequence's range of
   // tokens (a binary search over q_start is a chain of dependent loads).  The FP8-cache
   // instantiation runs at the register limit, where the lookup's extra live state cost more
@@ -357,17 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     len_b = p.seq_lens[b_seq];
   }
   const int L = min(len_b, p.max_pages * 64);  // positions the page table covers
-  // logical position -> physical row of every slot of this split (-1: empty or invalid)
-  // (all index loads of a thread first, then all page-table loads: two round trips)
+  // logical position -> physical row of every slot of this split (-1: empty or invalid): all
+  // page-table loads of a thread in flight together
   int last_valid = -1;
   {
-    constexpr int kPer = kMaxRows / kThreads;
-    int j[kPer], pg[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = u * kThreads + tid;
-      j[u] = i < nslot ? p.idx[(size_t)t * p.K + slot0 + i] : -1;
-    }
+    int pg[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u)
       pg[u] = (j[u] >= 0 && j[u] < L) ? p.page_table[(size_t)b_seq * p.max_pages + (j[u] >> 6)] : -1;
