@@ -100,7 +100,8 @@ def test_prolog_integer_inputs(cuda_lib, li_dtype):
 
 
 @pytest.mark.parametrize("n_new,d_q,d_model", [([1, 2, 3], 1536, 7168), ([150, 130, 20], 256, 512),
-                                               ([7], 72, 200)])
+                                               ([7], 72, 200), ([32], 1536, 7168),
+                                               ([300, 220], 1536, 7168)])
 def test_prolog_normal_inputs(cuda_lib, n_new, d_q, d_model):
     cpu, inp = _case("normal", "mxfp8", n_new=n_new, d_q=d_q, d_model=d_model,
                      seq_lens=[300, 4100, 65][:len(n_new)] if len(n_new) > 1 else [3000])
