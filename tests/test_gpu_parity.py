@@ -48,6 +48,20 @@ def test_integer_config_bit_exact(cuda_lib, lens, new):
     check_sfa(inp_cpu, g, toks)
 
 
+@pytest.mark.parametrize("K", [1, 17, 64, 200])
+def test_integer_config_small_k_bit_exact(cuda_lib, K):
+    """Top-K of one position, of fewer rows than one 64-row attention tile, of exactly one tile
+    and of a ragged number of tiles, beside a sequence of a single position: exact index sets,
+    and the attention reads only the selected rows."""
+    inp_cpu, inp = _small("decode_int_4k", seq_lens=[4096, 300, 1], n_new=[1, 2, 1], K=K)
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    toks = list(range(inp_cpu["wl"].n_q))
+    n_exact, ties = check_indices(inp_cpu, g, toks, exact=True)
+    assert n_exact == len(toks)
+    check_sfa(inp_cpu, g, toks)
+
+
 @pytest.mark.parametrize("lens,new", [([5000, 2100, 777], [1, 1, 1]), ([9000, 3000], [2, 2]),
                                       ([2047, 2048, 2049], [1, 2, 1])])
 def test_bf16_indexer_and_attention_small(cuda_lib, lens, new):
