@@ -429,3 +429,16 @@ def test_fp8_latent_cache_attention(cuda_lib, name, lens, new, prefill, K):
     toks = sample_tokens(inp_cpu["wl"], 12, seed=4)
     check_indices(inp_cpu, g, toks, exact=name == "decode_int_4k")
     check_sfa(inp_cpu, g, toks)
+
+
+@pytest.mark.parametrize("li_dtype", ["fp8", "mxfp8"])
+def test_quantised_indexer_with_fp8_latent_cache(cuda_lib, li_dtype):
+    """The fully quantised path: an e4m3 indexer (per-token or MX group scales) selects the rows
+    and the attention reads them from the FP8 latent cache; index sets are certified against the
+    oracle, and the output is checked on the GPU's own sets and end to end against the oracle's
+    selection and attention, within the FP8 indexer path's tolerance."""
+    inp_cpu, inp = _small("decode_32k_kv8", seq_lens=[5000, 2100, 777], n_new=[1, 2, 1],
+                          li_dtype=li_dtype)
+    g = run_gpu(inp)
+    assert g["status"] == 0
+    _check_path(inp_cpu, g, list(range(inp_cpu["wl"].n_q)), exact=False, tol=FP8_TOL)
