@@ -72,8 +72,12 @@ def test_bf16_indexer_and_attention_small(cuda_lib, lens, new):
     _check_path(inp_cpu, g, toks, exact=False)
 
 
-def test_fp8_integer_unit_case_bit_exact(cuda_lib):
-    inp_cpu, _ = _small("decode_32k_fp8", seq_lens=[6000, 2500, 300], n_new=[1, 2, 1])
+@pytest.mark.parametrize("lens,new", [([6000, 2500, 300], [1, 2, 1]), ([3000], [9]),
+                                      ([4100, 700], [5, 3])])
+def test_fp8_integer_unit_case_bit_exact(cuda_lib, lens, new):
+    """Per-token FP8: integer e4m3 codes with their per-token scales, for single tokens and for
+    groups of two and four tokens that share the key stream (each token's own query scale)."""
+    inp_cpu, _ = _small("decode_32k_fp8", seq_lens=lens, n_new=new)
     inp_cpu = integer_fp8(inp_cpu, seed=3)
     inp = di.to_device(inp_cpu, "cuda")
     g = run_gpu(inp)
